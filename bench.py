@@ -1,0 +1,479 @@
+"""Throughput bench of the exact attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--all]
+
+One step = one fa_fwd call over the whole workload (every (b, h) and every
+query row: the complete hot path).  Default workload: the causal bf16 d=128
+T=4096 point of the single-head sweep at B=64 (the shape the throughput target
+is stated on); Q, K, V are seeded N(0,1) synthetic tensors.  Prints ONE JSON
+line (rank 0):
+
+  value      TFLOP/s, flops = 4*B*Hq*T^2*d halved when causal, inputs resident
+             in HBM, CUDA events on the launching stream, max over ranks
+  e2e        the same metric with pinned-host inputs copied in and O, LSE
+             copied out inside every timed step (the public Python API)
+  roofline   the kernel against the measured bf16 dense peak (burst figure:
+             each launch is timed as a kernel of its own)
+  cpu_baseline  the fp64 CPU oracle, as it stands, on a bounded sample of the
+             same workload on this host's cores (rank 0, N=1 only)
+
+--impl reference times that oracle alone, as the reference arm, with the same
+metric, unit and config.  Under torchrun (N > 1) every rank runs its own
+replica of the workload on its own GPU (no collective on the data path):
+value = all ranks' flops / the slowest rank's time ("scaling": "weak").
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 BF16 dense peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129e6
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["fa_tc.cu", "ptx.cuh", "tc_layout.cuh", "wait.cuh", "fa_simt.cu", "fa_api.cu"]
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world: int, use_cuda: bool):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return dist
+
+
+def reduce_max(dist, x: float, device=None) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(values_per_rank_flops: float, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank's flops over the slowest rank's time."""
+    return values_per_rank_flops * world / max_seconds / 1e12
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_attention_90_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_tc_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split("=", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_per_launch_bytes"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        inside = [r for t, r in self.rows if t0 - 0.25 <= t <= t1 + 0.25]
+        note = None
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = [min(self.rows, key=lambda tr: abs(tr[0] - (t0 + t1) / 2))[1]]
+            note = "timed region shorter than the 200 ms sampling period: nearest sample"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, flag in zip(names, r[5:9]):
+                if flag.strip().lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "reasons": sorted(reasons), "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------- oracle timing
+def blas_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(w, budget_s: float):
+    """Times the fp64 oracle on whole (b, h) heads of the workload, one after
+    another, until about budget_s seconds have passed (at least one head).
+    Returns (TFLOP/s in the metric's causal-adjusted convention, sample text,
+    seconds)."""
+    import oracle
+    from exact_attention_90_gb300.inputs import make_qkv
+
+    q, k, v = make_qkv(1, 1, 1, w.T, w.d, dtype=w.dtype, seed=w.seed, mult=w.mult)
+    heads, t_total = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.attention_ref(q, k, v, w.scale, w.causal)
+        t_total += time.perf_counter() - t0
+        heads += 1
+        if t_total >= budget_s or heads >= w.B * w.Hq:
+            break
+    per_head = 4.0 * w.T * w.T * w.d / (2 if w.causal else 1)
+    value = heads * per_head / t_total / 1e12
+    sample = (f"{heads} whole head(s) of T={w.T} d={w.d} {w.dtype} "
+              f"{'causal' if w.causal else 'non-causal'} (1 of {w.B * w.Hq} heads each), "
+              f"{t_total:.1f} s")
+    return value, sample, t_total
+
+
+def time_oracle_rows(w, budget_s: float, seed: int):
+    """One reference-arm step: the oracle on a random set of query rows of the
+    workload, sized to take about budget_s seconds.  Returns (TFLOP/s, rows)."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_90_gb300.inputs import make_qkv
+
+    q, k, v = make_qkv(1, 1, 1, w.T, w.d, dtype=w.dtype, seed=w.seed, mult=w.mult)
+    rng = np.random.default_rng(seed)
+    rows_per_s = getattr(time_oracle_rows, "_rate", None)
+    if rows_per_s is None:
+        t0 = time.perf_counter()
+        oracle.attention_rows_ref(q, k, v, w.scale, w.causal, 0, 0, np.arange(64))
+        rows_per_s = 64 / max(time.perf_counter() - t0, 1e-6)
+        time_oracle_rows._rate = rows_per_s
+    n = int(max(16, min(w.T, rows_per_s * budget_s)))
+    rows = np.sort(rng.choice(w.T, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_rows_ref(q, k, v, w.scale, w.causal, 0, 0, rows)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * n * w.T * w.d / (2 if w.causal else 1)  # the rows' share of the head
+    return flops / dt / 1e12, n, dt
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    os.environ.setdefault("OMP_NUM_THREADS", str(blas_threads()))
+    step_budget = max(0.2, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        time_oracle_rows(w, step_budget, seed=i)
+    vals, rows_done, secs = [], 0, 0.0
+    for i in range(args.steps):
+        v, n, dt = time_oracle_rows(w, step_budget, seed=1000 + i)
+        vals.append(v)
+        rows_done += n
+        secs += dt
+    value = 4.0 * rows_done * w.T * w.d / (2 if w.causal else 1) / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} steps x ~{step_budget:.2f} s: random query "
+                                   f"rows of one head ({rows_done} rows in all)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, world):
+    in_bytes = (w.B * w.Hq + 2 * w.B * w.Hkv) * w.T * w.d * (2 if w.dtype == "bf16" else 4)
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "d": w.d,
+            "dtype": w.dtype, "causal": w.causal, "scale": w.scale,
+            "layout": "[B,H,T,d] contiguous",
+            "l2": (f"no flush: inputs {in_bytes / 2**20:.0f} MiB > 129 MB L2"
+                   if in_bytes > L2_BYTES else "L2 flushed between steps"),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def run_ours(args, w):
+    import torch
+
+    import exact_attention_90_gb300 as fa
+    from exact_attention_90_gb300.inputs import make_qkv
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = init_dist(world, True)
+    fa.load_library()  # raises if the CUDA library is missing: no fallback
+
+    qh, kh, vh = make_qkv(w.B, w.Hq, w.Hkv, w.T, w.d, dtype=w.dtype, seed=w.seed, mult=w.mult)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
+    in_bytes = sum(x.numel() * x.element_size() for x in (q, k, v))
+    flush = None if in_bytes > L2_BYTES else torch.empty(int(256e6), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if flush is not None:
+            flush.zero_()
+        st = fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.T, w.d, w.scale, int(w.causal),
+                       fa.FA_DTYPE_BF16 if w.dtype == "bf16" else fa.FA_DTYPE_F32, stream)
+        if st != 0:
+            raise fa.FaError(st, "fa_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_debug_sync_check(stream) != 0:
+        raise RuntimeError("kernel barrier wait timed out during warm-up")
+
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.3)
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = reduce_max(dist, ms, dev)
+    value = aggregate(w.flops * args.steps, world, ms_max / 1e3)
+    if fa.fa_debug_sync_check(stream) != 0:
+        raise RuntimeError("kernel barrier wait timed out during the timed region")
+
+    # ---- end to end: pinned host inputs in, O and LSE out, every step
+    e2e_steps = max(3, min(args.steps, 50))
+    qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
+    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
+    e2e_value = aggregate(w.flops * e2e_steps, world, e2e_ms / 1e3)
+    h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
+    d2h = op.numel() * op.element_size() + lp.numel() * lp.element_size()
+
+    peaks, src = load_peaks()
+    ms_per = ms / args.steps
+    achieved = w.flops / (ms_per / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"]) if w.dtype == "bf16" else None
+    traffic = ncu_traffic(w.name)
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q, K, V)",
+        "config": config_of(w, world),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (achieved / peak) if peak else None, "traffic": traffic,
+                     "peak_source": f"bf16_tflops (burst) of {src}",
+                     "algorithmic_flops_per_launch": w.flops,
+                     "algorithmic_bytes_per_launch": w.bytes,
+                     "hbm_gbs": w.bytes / (ms_per / 1e3) / 1e9,
+                     "hbm_frac": w.bytes / (ms_per / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                     "kernel": "fa_fwd_tc_kernel" if w.dtype == "bf16" else "fa_fwd_simt_kernel"},
+        "clocks": clocks,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        os.environ.setdefault("OMP_NUM_THREADS", str(blas_threads()))
+        cv, sample, _ = time_oracle(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": blas_threads(),
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_all(args):
+    """One line per workload (for the tables); not the headline contract."""
+    import torch
+
+    import exact_attention_90_gb300 as fa
+    from exact_attention_90_gb300.inputs import make_qkv
+    from exact_attention_90_gb300.workloads import all_workloads
+
+    fa.load_library()
+    peaks, src = load_peaks()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
+    for w in all_workloads():
+        if args.filter and args.filter not in w.name:
+            continue
+        q, k, v = (x.to(dev) for x in make_qkv(w.B, w.Hq, w.Hkv, w.T, w.d, dtype=w.dtype,
+                                               seed=w.seed, mult=w.mult))
+        o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(max(3, args.steps)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        tf = w.flops / (ms / 1e3) / 1e12
+        gbs = w.bytes / (ms / 1e3) / 1e9
+        print(json.dumps({"workload": w.name, "ms": ms, "tflops": tf,
+                          "frac_bf16_peak": tf / float(peaks["bf16_tflops"]),
+                          "hbm_gbs": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"]),
+                          "peaks": src, "l2": "flushed (256 MB write) before each call"}),
+              flush=True)
+        del q, k, v, o, lse
+    return 0
+
+
+def main(argv=None):
+    from exact_attention_90_gb300.workloads import HEADLINE, by_name
+
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--all", action="store_true", help="one line per workload shape")
+    ap.add_argument("--filter", default="", help="with --all: substring of workload names")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    _, _, world = dist_env()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    w = by_name(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    if args.all:
+        return run_all(args)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

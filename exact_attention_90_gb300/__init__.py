@@ -1,0 +1,210 @@
+"""Exact tiled attention forward for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libfa.so`` (C ABI in ``include/fa.h``).  It only
+marshals arguments: torch supplies device memory and the current stream,
+every step of the computation runs in the library's CUDA kernels.  There is no
+CPU fallback: if the shared library is missing or a call fails, an exception
+is raised.
+
+    import exact_attention_90_gb300 as fa
+    o, lse = fa.fwd(q, k, v, causal=True)          # q [B,Hq,T,d], k/v [B,Hkv,T,d]
+
+The operation (yelogs.com Flash Attention2/Triton tutorial, section "核心
+Kernel 實現"; "Flash Attention Memory Optimization Explained", section "What is
+Flash Attention?"): O = softmax(scale * Q K^T (+ causal mask)) V per
+(batch, head), and the row log-sum-exp L = m + ln l of the scaled, masked
+scores; query head h reads KV head h // (Hq // Hkv).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
+    "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
+    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "FA_DTYPE_F32", "FA_DTYPE_BF16",
+]
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+FA_DTYPE_F32 = 0
+FA_DTYPE_BF16 = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+# (name, restype, argtypes) of every exported symbol (include/fa.h, include/fa_unit.h)
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+EXPORTS = [
+    ("fa_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    ("fa_status_string", ctypes.c_char_p, [_I]),
+    ("fa_version", _I, []),
+    ("fa_debug_sync_check", _I, [_P]),
+    ("fa_last_cuda_error", _I, []),
+    ("fa_unit_tma", _I, [_P, _P, _I, _P]),
+    ("fa_unit_qk", _I, [_P, _P, _P, _I, _P]),
+    ("fa_unit_pv", _I, [_P, _P, _P, _P, _I, _I, ctypes.c_uint, ctypes.c_uint, _P]),
+    ("fa_fwd_simt", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+]
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _status_text(status)
+        if status == FA_ERR_CUDA and _LIB is not None:
+            msg += f" (cuda error {_LIB.fa_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libfa.so")
+
+
+def load_library():
+    """Loads libfa.so (built in-tree by ``build.py``); raises if it is absent."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m exact_attention_90_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, res, args in EXPORTS:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _status_text(s: int) -> str:
+    if _LIB is not None:
+        return _LIB.fa_status_string(int(s)).decode()
+    return f"status {s}"
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+# ------------------------------------------------------------------ raw C ABI
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, stream=None) -> int:
+    """The C function fa_fwd with the same arguments (tensors or raw device
+    pointers); returns the status code."""
+    lib = load_library()
+    return lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
+                      int(T), int(d), float(scale), int(causal), int(dtype), _stream(stream))
+
+
+def fa_fwd_simt(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, stream=None) -> int:
+    lib = load_library()
+    return lib.fa_fwd_simt(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                           int(Hkv), int(T), int(d), float(scale), int(causal), int(dtype),
+                           _stream(stream))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def fa_debug_sync_check(stream=None) -> int:
+    return load_library().fa_debug_sync_check(_stream(stream))
+
+
+def fa_last_cuda_error() -> int:
+    return load_library().fa_last_cuda_error()
+
+
+def fa_unit_tma(x, out, d, stream=None) -> int:
+    return load_library().fa_unit_tma(_ptr(x), _ptr(out), int(d), _stream(stream))
+
+
+def fa_unit_qk(q, k, s, d, stream=None) -> int:
+    return load_library().fa_unit_qk(_ptr(q), _ptr(k), _ptr(s), int(d), _stream(stream))
+
+
+def fa_unit_pv(p, pb, v, o, d, mode=0, lbo=0, sbo=0, stream=None) -> int:
+    return load_library().fa_unit_pv(_ptr(p), _ptr(pb), _ptr(v), _ptr(o), int(d), int(mode),
+                                     int(lbo), int(sbo), _stream(stream))
+
+
+# ------------------------------------------------------------------ tensor API
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+        stream=None, kernel: str = "auto"):
+    """Attention forward on CUDA tensors; returns (o, lse).
+
+    q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; all contiguous CUDA tensors of one
+    dtype (bfloat16 or float32).  scale defaults to 1/sqrt(d).  ``out`` and
+    ``lse`` may be given (shapes [B,Hq,T,d] in the input dtype and [B,Hq,T]
+    float32); otherwise they are allocated with torch.  ``kernel="simt"``
+    forces the fp32 CUDA-core kernel (also for bf16 inputs); the default picks
+    the kernel by dtype.  The call is asynchronous on ``stream`` (default: the
+    current torch stream).
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor [B, H, T, d]")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, T, d) or tuple(v.shape) != (B, Hkv, T, d):
+        raise ValueError(f"k, v must be [B, Hkv, T, d]; got {tuple(k.shape)}, {tuple(v.shape)}")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    call = fa_fwd_simt if kernel == "simt" else fa_fwd
+    if kernel not in ("auto", "simt"):
+        raise ValueError("kernel must be 'auto' or 'simt'")
+    st = call(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code, stream)
+    _check(st, "fa_fwd")
+    return out, lse

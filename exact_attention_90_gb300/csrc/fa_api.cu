@@ -1,0 +1,163 @@
+// fa_api.cu -- the C ABI of libfa.so: argument checks, tensor maps, dispatch.
+//
+// Entry points are declared (with their contracts) in include/fa.h and
+// include/fa_unit.h.  Nothing here allocates device memory or synchronises on
+// the fa_fwd path; errors are returned before anything is enqueued.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+fa_status tc_read_and_clear_error(unsigned int* word);    // fa_tc.cu
+fa_status unit_read_and_clear_error(unsigned int* word);  // fa_unit.cu
+
+static thread_local int t_last_cuda_error = 0;
+
+fa_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+fa_status cu_status(CUresult r) {
+  if (r == CUDA_SUCCESS) return FA_OK;
+  t_last_cuda_error = static_cast<int>(r);
+  return FA_ERR_CUDA;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+fa_status validate_fwd(const FwdArgs& a) {
+  if (!a.q || !a.k || !a.v || !a.o || !a.lse) return FA_ERR_INVALID_ARG;
+  if (a.B <= 0 || a.Hq <= 0 || a.Hkv <= 0 || a.T <= 0 || a.d <= 0) return FA_ERR_INVALID_ARG;
+  if (a.Hq % a.Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(a.scale)) return FA_ERR_INVALID_ARG;
+  if (a.causal != 0 && a.causal != 1) return FA_ERR_INVALID_ARG;
+  if (a.dtype != FA_DTYPE_F32 && a.dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  if (a.d != 16 && a.d != 32 && a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
+  // sizes: element counts must fit comfortably in 63 bits and the grid in 2^31
+  const double eq = static_cast<double>(a.B) * a.Hq * a.T * a.d;
+  if (eq > 9.0e15) return FA_ERR_INVALID_ARG;
+  const double units = static_cast<double>(a.B) * a.Hq * ((a.T + 63) / 64);
+  if (units > 2.0e9) return FA_ERR_INVALID_ARG;
+  if (static_cast<double>(a.B) * a.Hq > 2.0e9 || static_cast<double>(a.B) * a.Hkv > 2.0e9)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.o) ||
+      !aligned16(a.lse))
+    return FA_ERR_MISALIGNED;
+  const size_t e = a.dtype == FA_DTYPE_F32 ? 4 : 2;
+  const size_t nq = static_cast<size_t>(a.B) * a.Hq * a.T * a.d * e;
+  const size_t nkv = static_cast<size_t>(a.B) * a.Hkv * a.T * a.d * e;
+  const size_t nl = static_cast<size_t>(a.B) * a.Hq * a.T * 4;
+  if (overlap(a.o, nq, a.q, nq) || overlap(a.o, nq, a.k, nkv) || overlap(a.o, nq, a.v, nkv) ||
+      overlap(a.o, nq, a.lse, nl) || overlap(a.lse, nl, a.q, nq) || overlap(a.lse, nl, a.k, nkv) ||
+      overlap(a.lse, nl, a.v, nkv))
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static CUresult g_encode_status = CUDA_ERROR_NOT_INITIALIZED;
+static std::once_flag g_encode_once;
+
+static void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    g_encode_status = CUDA_ERROR_NOT_FOUND;
+    return;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  g_encode_status = CUDA_SUCCESS;
+}
+
+CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long long BH, int box_x,
+                        int swizzle) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode_status != CUDA_SUCCESS) return g_encode_status;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  static_cast<CUtensorMapSwizzle>(swizzle), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  unsigned int a = 0, b = 0;
+  fa_status s = tc_read_and_clear_error(&a);
+  if (s != FA_OK) return s;
+  s = unit_read_and_clear_error(&b);
+  if (s != FA_OK) return s;
+  *word = a | b;
+  return FA_OK;
+}
+
+}  // namespace fa
+
+// ---------------------------------------------------------------- C ABI
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int T, int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype,
+                static_cast<cudaStream_t>(stream)};
+  fa_status s = fa::validate_fwd(a);
+  if (s != FA_OK) return s;
+  return dtype == FA_DTYPE_BF16 ? fa::launch_tc(a) : fa::launch_simt(a);
+}
+
+fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int T, int d, float scale, int causal, fa_dtype dtype,
+                      void* stream) {
+  fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype,
+                static_cast<cudaStream_t>(stream)};
+  fa_status s = fa::validate_fwd(a);
+  if (s != FA_OK) return s;
+  return fa::launch_simt(a);
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_version(void) { return 10000; }
+
+int fa_last_cuda_error(void) { return fa::t_last_cuda_error; }
+
+fa_status fa_debug_sync_check(void* stream) {
+  unsigned int word = 0;
+  fa_status s = fa::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &word);
+  if (s != FA_OK) return s;
+  return word ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

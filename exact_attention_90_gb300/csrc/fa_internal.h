@@ -1,0 +1,45 @@
+// fa_internal.h -- declarations shared by the translation units of libfa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, T, d;
+  float scale;
+  int causal;
+  fa_dtype dtype;
+  cudaStream_t stream;
+};
+
+// Host-side argument checks shared by every entry point (no CUDA calls).
+fa_status validate_fwd(const FwdArgs& a);
+
+// Records a CUDA error for fa_last_cuda_error() and maps it to a status.
+fa_status cuda_status(cudaError_t e);
+fa_status cu_status(CUresult r);
+
+// 3-D bf16 tensor map over a contiguous [BH][T][d] tensor with boxes of
+// box_x columns x 128 rows x 1 and the given swizzle (CUtensorMapSwizzle).
+CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long long BH,
+                        int box_x, int swizzle);
+
+// Kernel launchers (enqueue only; arguments already validated).
+fa_status launch_tc(const FwdArgs& a);    // bf16, tcgen05
+fa_status launch_simt(const FwdArgs& a);  // fp32 or bf16, CUDA cores
+
+// Device error word shared by the kernels (read-and-clear, synchronous).
+fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
+
+}  // namespace fa

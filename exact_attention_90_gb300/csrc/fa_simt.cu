@@ -1,0 +1,301 @@
+// fa_simt.cu -- true-fp32 exact attention forward on the CUDA cores.
+//
+// The same computation as the tensor-core kernel (see fa_tc.cu): the tiled
+// forward with online softmax of the yelogs.com Flash Attention2/Triton
+// tutorial, section "核心 Kernel 實現" -- Q block kept on chip, K/V blocks
+// streamed, running max m, normaliser l and output accumulator in fp32, the
+// accumulator rescaled by exp(m_old - m_new) per block (section "Softmax 的在線
+// 計算"), O / l and L = m + log l at the end -- with every product done by FFMA
+// in fp32.  fp32 inputs need this path: a TF32 tensor-core product would not
+// keep O within 1e-4 of the exact result.  It also accepts bf16 inputs (fp32
+// arithmetic), which the tests use as a cross-check of the tensor-core kernel.
+//
+// CTA = 128 threads = a 16 x 8 grid (tx, ty) over a 64-query x 64-key block:
+// thread (tx, ty) owns query rows ty*8 .. ty*8+7, score columns tx*4 .. tx*4+3
+// and d/16 output columns; row maxima and sums combine the 16 threads of a row
+// with warp shuffles.  Tiles live in shared memory with padded rows so the
+// 16-byte loads of a quarter-warp hit distinct banks.
+#include <cmath>
+
+#include "fa_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace fa {
+
+namespace {
+
+constexpr int BQ = 64;
+constexpr int BK = 64;
+
+template <int D>
+struct SimtCfg {
+  static constexpr int QS = D + 4;  // padded row stride (floats) of Q and K
+  static constexpr int PS = BK + 4; // padded row stride of P
+  static constexpr int OC = D / 16; // output columns per thread
+  static constexpr int SMEM_FLOATS = BQ * QS + BK * QS + BK * D + BQ * PS;
+  static constexpr int SMEM_BYTES = SMEM_FLOATS * 4;
+};
+
+// Output column of a thread's c-th accumulator.
+template <int D>
+__device__ __forceinline__ int ocol(int tx, int c) {
+  if constexpr (D >= 64) return tx * 4 + 64 * (c / 4) + (c % 4);
+  else if constexpr (D == 32) return tx * 2 + c;
+  else return tx;
+}
+
+// rows [r0, r0+64) of a [T][D] matrix into smem (row stride LS floats); rows
+// at or past T become zero
+template <int D, int LS>
+__device__ __forceinline__ void load_tile(float* dst, const float* src, int r0, int T) {
+  constexpr int V = D / 4;  // float4 per row
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < 64 * V; idx += 128) {
+    const int r = idx / V, c4 = idx % V;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + r < T) x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(r0 + r) * D) + c4);
+    *reinterpret_cast<float4*>(dst + r * LS + 4 * c4) = x;
+  }
+}
+
+template <int D, int LS>
+__device__ __forceinline__ void load_tile(float* dst, const __nv_bfloat16* src, int r0, int T) {
+  constexpr int V = D / 8;  // 16-byte vectors of 8 bf16 per row
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < 64 * V; idx += 128) {
+    const int r = idx / V, c8 = idx % V;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < T) x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r0 + r) * D) + c8);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[2 * e] = __uint_as_float(w[e] << 16);
+      f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+    float* d = dst + r * LS + 8 * c8;
+    *reinterpret_cast<float4*>(d) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4*>(d + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+__device__ __forceinline__ void store_out(float* dst, const float* x, int n) {
+  if (n == 4) *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+  else if (n == 2) *reinterpret_cast<float2*>(dst) = make_float2(x[0], x[1]);
+  else dst[0] = x[0];
+}
+
+__device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float* x, int n) {
+  if (n == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else if (n == 2) {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(x[0], x[1]);
+  } else {
+    dst[0] = __float2bfloat16_rn(x[0]);
+  }
+}
+
+template <typename Tin, int D, bool CAUSAL>
+__global__ void __launch_bounds__(128)
+    fa_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                       const Tin* __restrict__ v, Tin* __restrict__ o, float* __restrict__ lse,
+                       int B, int Hq, int Hkv, int T, float scale) {
+  using C = SimtCfg<D>;
+  constexpr int QS = C::QS, PS = C::PS, OC = C::OC;
+  constexpr int GW = D >= 64 ? 4 : (D == 32 ? 2 : 1);  // contiguous output columns
+  extern __shared__ float4 smem4[];
+  float* sQ = reinterpret_cast<float*>(smem4);
+  float* sK = sQ + BQ * QS;
+  float* sV = sK + BK * QS;
+  float* sP = sV + BK * D;
+
+  const int tid = threadIdx.x;
+  const int ty = tid >> 4, tx = tid & 15;
+  const int BH = B * Hq;
+  const int n_qt = (T + BQ - 1) / BQ;
+  const int n_kt = (T + BK - 1) / BK;
+  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // longest blocks first
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int b = bh / Hq, h = bh - (bh / Hq) * Hq;
+  const int hk = h / (Hq / Hkv);
+  const int q0 = qt * BQ;
+  const size_t qoff = static_cast<size_t>(bh) * T * D;
+  const size_t kvoff = static_cast<size_t>(b * Hkv + hk) * T * D;
+
+  load_tile<D, QS>(sQ, q + qoff, q0, T);
+
+  float m[8], lp[8], acc[8][OC];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    m[i] = -INFINITY;
+    lp[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < OC; ++c) acc[i][c] = 0.f;
+  }
+
+  const int n_kv = CAUSAL ? min(n_kt, (q0 + BQ - 1) / BK + 1) : n_kt;
+  for (int j = 0; j < n_kv; ++j) {
+    __syncthreads();  // previous block's K, V, P no longer in use
+    load_tile<D, QS>(sK, k + kvoff, j * BK, T);
+    load_tile<D, D>(sV, v + kvoff, j * BK, T);
+    __syncthreads();
+
+    // S = Q K^T for the thread's 8 x 4 scores
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[i][c] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < D; kk += 4) {
+      float4 kv[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        kv[c] = *reinterpret_cast<const float4*>(sK + (tx * 4 + c) * QS + kk);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 qv = *reinterpret_cast<const float4*>(sQ + (ty * 8 + i) * QS + kk);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          s[i][c] = fmaf(qv.x, kv[c].x, s[i][c]);
+          s[i][c] = fmaf(qv.y, kv[c].y, s[i][c]);
+          s[i][c] = fmaf(qv.z, kv[c].z, s[i][c]);
+          s[i][c] = fmaf(qv.w, kv[c].w, s[i][c]);
+        }
+      }
+    }
+
+    // scale, mask, online softmax update.  Natural-log units: the running
+    // maximum m is a rounded scaled score, and every exponent argument
+    // s * scale - m is formed by one fused multiply-add, so m's own rounding
+    // cancels between l and L = m + ln l.
+    const int kb = j * BK + tx * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = q0 + ty * 8 + i;
+      bool keep[4];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = kb + c;
+        keep[c] = key < T && (!CAUSAL || key <= row);
+        if (keep[c]) mx = fmaxf(mx, s[i][c] * scale);
+      }
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m[i], mx);
+      const float mo = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = expf(m[i] - mo);  // 0 while m[i] = -inf
+      float p[4], ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        p[c] = keep[c] ? expf(fmaf(s[i][c], scale, -mo)) : 0.f;
+        ps += p[c];
+      }
+      lp[i] = lp[i] * alpha + ps;
+#pragma unroll
+      for (int c = 0; c < OC; ++c) acc[i][c] *= alpha;
+      m[i] = m_new;
+      *reinterpret_cast<float4*>(sP + (ty * 8 + i) * PS + tx * 4) = make_float4(p[0], p[1], p[2], p[3]);
+    }
+    __syncthreads();
+
+    // O += P V
+#pragma unroll 2
+    for (int kk = 0; kk < BK; kk += 4) {
+      float4 pv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pv[i] = *reinterpret_cast<const float4*>(sP + (ty * 8 + i) * PS + kk);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float vv[OC];
+        const float* vr = sV + (kk + u) * D;
+#pragma unroll
+        for (int c = 0; c < OC; c += GW) {
+          if constexpr (GW == 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(vr + ocol<D>(tx, c));
+            vv[c] = t4.x; vv[c + 1] = t4.y; vv[c + 2] = t4.z; vv[c + 3] = t4.w;
+          } else if constexpr (GW == 2) {
+            const float2 t2 = *reinterpret_cast<const float2*>(vr + ocol<D>(tx, c));
+            vv[c] = t2.x; vv[c + 1] = t2.y;
+          } else {
+            vv[c] = vr[ocol<D>(tx, c)];
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float pu = u == 0 ? pv[i].x : (u == 1 ? pv[i].y : (u == 2 ? pv[i].z : pv[i].w));
+#pragma unroll
+          for (int c = 0; c < OC; ++c) acc[i][c] = fmaf(pu, vv[c], acc[i][c]);
+        }
+      }
+    }
+  }
+
+  // normalise and store
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float l = lp[i];
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    const int row = q0 + ty * 8 + i;
+    if (row < T) {
+      const float inv = 1.f / l;
+      Tin* orow = o + qoff + static_cast<size_t>(row) * D;
+#pragma unroll
+      for (int c = 0; c < OC; c += GW) {
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < GW; ++e) y[e] = acc[i][c + e] * inv;
+        store_out(orow + ocol<D>(tx, c), y, GW);
+      }
+      if (tx == 0) lse[static_cast<size_t>(bh) * T + row] = m[i] + logf(l);
+    }
+  }
+}
+
+template <typename Tin, int D, bool CAUSAL>
+fa_status launch_simt_impl(const FwdArgs& a) {
+  using C = SimtCfg<D>;
+  auto kern = fa_fwd_simt_kernel<Tin, D, CAUSAL>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_status(e);
+    attr_done = true;
+  }
+  const long long blocks = static_cast<long long>(a.B) * a.Hq * ((a.T + BQ - 1) / BQ);
+  kern<<<static_cast<unsigned>(blocks), 128, C::SMEM_BYTES, a.stream>>>(
+      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
+      static_cast<Tin*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, a.scale);
+  return cuda_status(cudaGetLastError());
+}
+
+template <typename Tin>
+fa_status launch_simt_t(const FwdArgs& a) {
+  const bool c = a.causal != 0;
+  switch (a.d) {
+    case 16: return c ? launch_simt_impl<Tin, 16, true>(a) : launch_simt_impl<Tin, 16, false>(a);
+    case 32: return c ? launch_simt_impl<Tin, 32, true>(a) : launch_simt_impl<Tin, 32, false>(a);
+    case 64: return c ? launch_simt_impl<Tin, 64, true>(a) : launch_simt_impl<Tin, 64, false>(a);
+    case 128: return c ? launch_simt_impl<Tin, 128, true>(a) : launch_simt_impl<Tin, 128, false>(a);
+    default: return FA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+fa_status launch_simt(const FwdArgs& a) {
+  if (a.dtype == FA_DTYPE_F32) return launch_simt_t<float>(a);
+  if (a.dtype == FA_DTYPE_BF16) return launch_simt_t<__nv_bfloat16>(a);
+  return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

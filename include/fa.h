@@ -1,0 +1,97 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention forward for GB300 (sm_103a).
+ *
+ * The operation (sources are web pages, cited by page and section):
+ *   "Flash Attention Memory Optimization Explained" (lzwjava.github.io),
+ *   section "What is Flash Attention?": an exact scaled dot-product attention
+ *   that never stores the T x T score matrix; the yelogs.com Flash
+ *   Attention2/Triton tutorial, sections "核心 Kernel 實現" (tiled forward with
+ *   online softmax that writes O and the per-row L), "Softmax 的在線計算"
+ *   (running max m and normaliser l) and "2. 多查詢注意力（MQA）" (one KV head
+ *   shared by all query heads).
+ *
+ *   For batch b, query head h, KV head hk = h / (Hq / Hkv), query row i:
+ *     S[i][j] = scale * dot(Q[b][h][i][:], K[b][hk][j][:])
+ *     keys j  = 0..T-1, or only j <= i when causal
+ *     O[b][h][i][:] = sum_j softmax_j(S[i][:]) * V[b][hk][j][:]
+ *     lse[b][h][i]  = m_i + ln(l_i)  (m_i = max_j S[i][j],
+ *                                    l_i = sum_j exp(S[i][j] - m_i))
+ *
+ * Memory: every buffer is a DEVICE pointer owned by the caller; the library
+ * never allocates, frees or keeps them.  Layouts are contiguous row-major:
+ *   q   [B][Hq][T][d]    element type `dtype`
+ *   k,v [B][Hkv][T][d]   element type `dtype`
+ *   o   [B][Hq][T][d]    element type `dtype` (written; round-to-nearest-even)
+ *   lse [B][Hq][T]       float32 (written; natural log)
+ * o and lse must not overlap each other or the inputs.  All pointers must be
+ * 16-byte aligned.
+ *
+ * Execution: fa_fwd validates its arguments on the host, then enqueues one
+ * kernel on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ * returns without synchronising.  No host synchronisation and no device
+ * allocation happen on this path.  The current CUDA device must be the one
+ * that owns the buffers.
+ *
+ * Kernels by dtype (selection by the arithmetic type, not a fallback):
+ *   FA_DTYPE_BF16: TMA-staged swizzled tiles, tcgen05 MMA into tensor memory,
+ *                  warp-specialised softmax (d in {16, 32, 64, 128});
+ *   FA_DTYPE_F32 : true-fp32 FFMA kernel on the CUDA cores (same d).
+ * Dropout and arbitrary attention masks are not supported.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, size <= 0, Hq % Hkv != 0,
+                             non-finite scale, causal not 0/1, overlap of an
+                             output with another buffer, size overflow */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {16,32,64,128} or unknown dtype */
+  FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch etc.) */
+  FA_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a barrier (reported
+                             by fa_debug_sync_check only) */
+} fa_status;
+
+typedef enum { FA_DTYPE_F32 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
+
+/* Exact attention forward with log-sum-exp (see the header comment).
+ *   q, k, v : device inputs; o, lse : device outputs
+ *   B, Hq, Hkv, T, d : sizes (> 0; Hq a multiple of Hkv; d in {16,32,64,128})
+ *   scale   : finite multiplier of every score (1/sqrt(d) is the usual one)
+ *   causal  : 1 keeps key j for query i only when j <= i; 0 keeps all
+ *   dtype   : element type of q, k, v and o
+ *   stream  : cudaStream_t to enqueue on
+ * Returns FA_OK once the kernel is enqueued; on any error nothing is
+ * launched and the outputs are untouched. */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                 fa_dtype dtype, void* stream);
+
+/* Static English text for a status code (never NULL). */
+const char* fa_status_string(fa_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+/* Debug/test aid, not for the hot path: synchronises `stream`, then reads and
+ * clears the device-side error word that kernels set when a barrier wait runs
+ * out of time (each wait is bounded; on expiry the kernel abandons its work,
+ * frees its tensor memory and exits instead of hanging).  Returns
+ * FA_ERR_TIMEOUT if the word was set, FA_ERR_CUDA if the synchronisation
+ * failed, else FA_OK. */
+fa_status fa_debug_sync_check(void* stream);
+
+/* Last CUDA error code seen by the library on this thread (0 if none);
+ * detail for FA_ERR_CUDA. */
+int fa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,135 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+headers declare, and rejects bad arguments on the host before any CUDA call
+(so these run on a machine with no driver)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_90_gb300 as fa
+from exact_attention_90_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(INCLUDE):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(INCLUDE, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_the_abi():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_status_string", "fa_version", "fa_debug_sync_check",
+              "fa_last_cuda_error", "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_fwd_simt"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libfa.so does not export {n}"
+    # and the binding wraps each of them under the same name
+    wrapped = {name for name, _, _ in fa.EXPORTS}
+    assert set(declared_functions()) <= wrapped
+    for n in declared_functions():
+        assert callable(getattr(fa, n))
+
+
+def test_version_and_status_strings(lib):
+    assert fa.fa_version() == 10000
+    for s in range(6):
+        txt = fa.fa_status_string(s)
+        assert isinstance(txt, str) and txt
+    assert fa.fa_status_string(0) == "ok"
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+# fake, 16-byte aligned, far-apart device addresses: validation never touches them
+BASE = 1 << 44
+Q, K, V, O, L = (BASE + (i << 36) for i in range(5))
+GOOD = dict(q=Q, k=K, v=V, o=O, lse=L, B=2, Hq=4, Hkv=2, T=100, d=64, scale=0.125, causal=1,
+            dtype=fa.FA_DTYPE_BF16)
+
+
+def call(**kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                     a["T"], a["d"], a["scale"], a["causal"], a["dtype"], stream=0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(k=0), fa.FA_ERR_INVALID_ARG),
+    (dict(v=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Hq=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(T=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Hq=4, Hkv=3), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(d=48), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=Q + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o=O + 4), fa.FA_ERR_MISALIGNED),
+    (dict(lse=L + 2), fa.FA_ERR_MISALIGNED),
+    (dict(o=Q), fa.FA_ERR_INVALID_ARG),          # output aliases an input
+    (dict(o=K + 4096), fa.FA_ERR_INVALID_ARG),   # output overlaps K
+    (dict(lse=O + 64), fa.FA_ERR_INVALID_ARG),   # the two outputs overlap
+    (dict(B=1 << 20, Hq=1 << 12, Hkv=1 << 12, T=1 << 20), fa.FA_ERR_INVALID_ARG),  # size overflow
+])
+def test_fwd_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert call(**kw) == status
+    # same checks for the CUDA-core entry point
+    a = dict(GOOD)
+    a.update(kw)
+    assert fa.fa_fwd_simt(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                          a["T"], a["d"], a["scale"], a["causal"], a["dtype"], stream=0) == status
+
+
+def test_unit_entry_points_reject_bad_arguments(lib):
+    assert fa.fa_unit_tma(0, O, 64, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_tma(Q, O, 48, stream=0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_unit_tma(Q + 4, O, 64, stream=0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_unit_qk(Q, 0, O, 64, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_qk(Q, K, O, 8, stream=0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_unit_pv(Q, 0, K, 0, 64, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pv(Q, 0, K, O, 64, mode=4, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pv(0, 0, K, O, 64, mode=0, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pv(Q, 0, K, O, 64, mode=2, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pv(Q, 0, K, O, 64, lbo=8, stream=0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_tensor_api_refuses_cpu_tensors():
+    import torch
+
+    q = torch.zeros(1, 1, 8, 16)
+    with pytest.raises(TypeError):
+        fa.fwd(q, q, q)
+
+
+def test_exported_symbols_have_c_linkage(lib):
+    # a C++-mangled name would not be found by its plain name
+    for n in declared_functions():
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
