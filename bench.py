@@ -27,6 +27,7 @@ value = all ranks' flops / the slowest rank's time ("scaling": "weak").
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -315,6 +316,14 @@ def run_ours(args, w):
     if fa.fa_debug_sync_check(stream) != 0:
         raise RuntimeError("kernel barrier wait timed out during warm-up")
 
+    if args.profile:
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize(dev)
+        st = fa.fa_debug_sync_check(stream)
+        print(json.dumps({"profile": w.name, "steps": args.steps, "status": st}), flush=True)
+        return 0 if st == 0 else 1
+
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                            if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local_rank)
     sampler.start()
@@ -452,7 +461,7 @@ def main(argv=None):
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
@@ -461,6 +470,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="device steps only (no e2e, oracle or clock sampling): for ncu")
+    ap.add_argument("--B", type=int, default=0, help="override the workload's batch size")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -468,6 +480,8 @@ def main(argv=None):
     if world != args.gpus and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     w = by_name(args.workload)
+    if args.B:
+        w = dataclasses.replace(w, B=args.B, name=f"{w.name}@B{args.B}")
     if args.impl == "reference":
         return run_reference(args, w)
     if args.all:

@@ -25,7 +25,8 @@ import os
 __all__ = [
     "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
-    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "FA_DTYPE_F32", "FA_DTYPE_BF16",
+    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "FA_DTYPE_F32",
+    "FA_DTYPE_BF16",
 ]
 
 FA_OK = 0
@@ -51,6 +52,7 @@ EXPORTS = [
     ("fa_unit_tma", _I, [_P, _P, _I, _P]),
     ("fa_unit_qk", _I, [_P, _P, _P, _I, _P]),
     ("fa_unit_pv", _I, [_P, _P, _P, _P, _I, _I, ctypes.c_uint, ctypes.c_uint, _P]),
+    ("fa_unit_timeout", _I, [ctypes.c_longlong, _P, _P]),
     ("fa_fwd_simt", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
 ]
 
@@ -157,6 +159,10 @@ def fa_unit_qk(q, k, s, d, stream=None) -> int:
 def fa_unit_pv(p, pb, v, o, d, mode=0, lbo=0, sbo=0, stream=None) -> int:
     return load_library().fa_unit_pv(_ptr(p), _ptr(pb), _ptr(v), _ptr(o), int(d), int(mode),
                                      int(lbo), int(sbo), _stream(stream))
+
+
+def fa_unit_timeout(budget_cycles, gave_up, stream=None) -> int:
+    return load_library().fa_unit_timeout(int(budget_cycles), _ptr(gave_up), _stream(stream))
 
 
 # ------------------------------------------------------------------ tensor API

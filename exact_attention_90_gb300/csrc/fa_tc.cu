@@ -18,6 +18,8 @@
 //   warps 4-7 : the same for Q1
 //   warp 8    : TMA producer (Q0, Q1 once; K_j, V_j through an NS-deep ring)
 //   warp 9    : MMA issuer (one thread)
+//   warps 10-11 complete the third warpgroup, whose registers setmaxnreg
+//   hands to the two softmax warpgroups
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  fp32 scores of Q0 K_j^T, Q1 K_j^T
 //   P0, P1      bf16 probabilities packed two per column in the first 64
@@ -44,12 +46,29 @@ namespace fa {
 
 static __device__ unsigned int g_tc_err;
 
+// Tuning parameters (compile-time; defaults are the measured best):
+//   FA_TC_P_CHUNKS   -- P is released to the MMA thread in this many pieces
+//   FA_TC_REG_SPLIT  -- 1: 384 threads, setmaxnreg moves registers from the
+//                       load/MMA warpgroup to the softmax warpgroups;
+//                       0: 320 threads, one register budget for all warps
+#ifndef FA_TC_P_CHUNKS
+#define FA_TC_P_CHUNKS 4
+#endif
+#ifndef FA_TC_REG_SPLIT
+#define FA_TC_REG_SPLIT 1
+#endif
+
 template <int D>
 struct TcCfg : TcTile<D> {
   using Tile = TcTile<D>;
   static constexpr int NS = D == 128 ? 2 : 4;  // K/V ring depth
-  static constexpr int THREADS = 320;
-  static constexpr int SMEM_BYTES = 1024 + (2 + 2 * NS) * Tile::TILE_BYTES + 256;
+  static constexpr int THREADS = FA_TC_REG_SPLIT ? 384 : 320;  // softmax Q0, Q1; load/MMA
+  static constexpr int REGS_SOFTMAX = 200;  // per thread after setmaxnreg, warpgroups 0 and 1
+  static constexpr int REGS_OTHER = 88;     // warpgroup 2
+  static constexpr int P_CHUNKS = FA_TC_P_CHUNKS;  // P released to the MMA in key chunks
+  // registers the three warpgroups hold after reallocation
+  static constexpr int REGS_SPLIT = FA_TC_REG_SPLIT ? 128 * (2 * REGS_SOFTMAX + REGS_OTHER) : 0;
+  static constexpr int SMEM_BYTES = 1024 + (2 + 2 * NS) * Tile::TILE_BYTES + 512;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
 };
@@ -58,7 +77,7 @@ struct TcCfg : TcTile<D> {
 #define FA_RESCALE_THRESHOLD 8.0f
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
@@ -80,8 +99,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* bar_vfull = bar_kfull + NS;
   uint64_t* bar_kvempty = bar_vfull + NS;
   uint64_t* bar_sfull = bar_kvempty + NS;  // [2]
-  uint64_t* bar_pfull = bar_sfull + 2;     // [2]
-  uint64_t* bar_odone = bar_pfull + 2;     // [2]
+  uint64_t* bar_pfull = bar_sfull + 2;     // [2][P_CHUNKS]
+  uint64_t* bar_odone = bar_pfull + 2 * C::P_CHUNKS;  // [2]
   uint64_t* bar_final = bar_odone + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -99,13 +118,13 @@ __global__ void __launch_bounds__(320, 1)
   const int hk = h / (Hq / Hkv);
   const int q0 = qb * 256;
   const int n_kv_all = (T + 127) >> 7;
-  int n_t[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
+  // KV tiles each Q tile visits (0 if the tile lies past T)
+  auto n_of = [&](int t) {
     const int qs = q0 + 128 * t;
-    n_t[t] = qs >= T ? 0 : (CAUSAL ? min(n_kv_all, (qs >> 7) + 1) : n_kv_all);
-  }
-  const int n_kv = max(n_t[0], n_t[1]);
+    return qs >= T ? 0 : (CAUSAL ? min(n_kv_all, (qs >> 7) + 1) : n_kv_all);
+  };
+  const int n_t0 = n_of(0), n_t1 = n_of(1);
+  const int n_kv = max(n_t0, n_t1);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_q, 1);
@@ -116,7 +135,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bar_sfull[t], 1);
-      ptx::mbar_init(&bar_pfull[t], 128);
+      for (int c = 0; c < C::P_CHUNKS; ++c) ptx::mbar_init(&bar_pfull[t * C::P_CHUNKS + c], 4);
       ptx::mbar_init(&bar_odone[t], 1);
     }
     ptx::mbar_init(bar_final, 1);
@@ -132,7 +151,21 @@ __global__ void __launch_bounds__(320, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  // every role ends here: all tensor-memory traffic is done before warp 0
+  // frees the columns
+  auto teardown = [&]() {
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  };
+
+  // Each warpgroup's code lives entirely inside its own branch (no code after
+  // the branches), so every region compiles under its own register budget.
+  if (warp >= 8) {
+    // ================================================ warpgroup 2: load, MMA
+    if constexpr (FA_TC_REG_SPLIT) ptx::setmaxnreg_dec<C::REGS_OTHER>();
+    if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       ptx::prefetch_tmap(&tmQ);
@@ -174,7 +207,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+    } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 128, false, false);
@@ -199,29 +232,40 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
 
-      if (ok && n_t[0] > 0) ok = issue_s(0, 0);
-      if (ok && n_t[1] > 0) ok = issue_s(1, 0);
+      if (ok && n_t0 > 0) ok = issue_s(0, 0);
+      if (ok && n_t1 > 0) ok = issue_s(1, 0);
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % NS;
         if (!wait_bar(&bar_vfull[st], (j / NS) & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
         ptx::tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int t = 0; t < 2; ++t) {
-          if (ok && j < n_t[t]) {
-            if (!wait_bar(&bar_pfull[t], j & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
+          const int nt = t == 0 ? n_t0 : n_t1;
+          if (ok && j < nt) {
+            // P arrives in chunks of 32 keys (two k-steps each): the tensor
+            // core starts on the first chunk while the rest is computed
 #pragma unroll
-            for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
-              ptx::mma_ts(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
-                          Tile::mnmajor_desc(aV + st * TILE, kk), IDESC_PV,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+            for (int c = 0; c < C::P_CHUNKS; ++c) {
+              if (!wait_bar(&bar_pfull[t * C::P_CHUNKS + c], j & 1, abort_flag, &g_tc_err,
+                            kErrWaitMma)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              constexpr int KPC = Tile::PV_KSTEPS / C::P_CHUNKS;
+#pragma unroll
+              for (int kq = 0; kq < KPC; ++kq) {
+                const int kk = c * KPC + kq;
+                ptx::mma_ts(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
+                            Tile::mnmajor_desc(aV + st * TILE, kk), IDESC_PV,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
             ptx::mma_commit(&bar_odone[t]);
-            const bool last_pv = (t == 1) || !(j < n_t[1]);
+            const bool last_pv = (t == 1) || !(j < n_t1);
             if (last_pv) ptx::mma_commit(&bar_kvempty[st]);
-            if (j + 1 < n_t[t]) ok = issue_s(t, j + 1);
+            if (j + 1 < nt) ok = issue_s(t, j + 1);
           }
         }
       }
@@ -229,8 +273,11 @@ __global__ void __launch_bounds__(320, 1)
       drain_bar(bar_final, 0, &g_tc_err);
     }
     __syncwarp();
+    }
+    teardown();
   } else {
-    // ------------------------------------------------------------ softmax
+    // ================================================ warpgroups 0, 1: softmax
+    if constexpr (FA_TC_REG_SPLIT) ptx::setmaxnreg_inc<C::REGS_SOFTMAX>();
     const int t = warp >> 2;
     const int qr = warp & 3;
     const int row = qr * 32 + lane;
@@ -239,7 +286,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(qr * 32) << 16;
     const uint32_t tS = tmem + C::COL_S0 + t * 128 + lane_off;
     const uint32_t tO = tmem + C::COL_O0 + t * 128 + lane_off;
-    const int n = n_t[t];
+    const int n = t == 0 ? n_t0 : n_t1;
     const bool neg = scale_log2 < 0.f;
     const float mask_val = neg ? INFINITY : -INFINITY;
     float m_ref = -INFINITY;
@@ -260,19 +307,16 @@ __global__ void __launch_bounds__(320, 1)
       ptx::reg_fence(s[2]);
       ptx::reg_fence(s[3]);
 
+      // masked scores become -inf (+inf when scale < 0), so that their
+      // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is never
+      // 0: the host passes the smallest normal float for scale = 0)
       const int kb = j * 128;
       const bool masked = (kb + 127 >= T) || (CAUSAL && kb + 127 > q_start);
-      uint32_t vbits[4] = {~0u, ~0u, ~0u, ~0u};
       if (masked) {
+        const int lim = CAUSAL ? min(T - 1, grow) - kb : T - 1 - kb;  // last kept column
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int key = kb + c;
-          const bool keep = key < T && (!CAUSAL || key <= grow);
-          if (!keep) {
-            s[c >> 5][c & 31] = __float_as_uint(mask_val);
-            vbits[c >> 5] &= ~(1u << (c & 31));
-          }
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c >> 5][c & 31] = __float_as_uint(mask_val);
       }
       float mx;
       if (!neg) {
@@ -306,25 +350,8 @@ __global__ void __launch_bounds__(320, 1)
         m_ref = m_cand;
       }
       const float mo = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * u]), scale_log2, -mo));
-          float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * u + 1]), scale_log2, -mo));
-          if (masked) {
-            p0 = ((vbits[c] >> (2 * u)) & 1u) ? p0 : 0.f;
-            p1 = ((vbits[c] >> (2 * u + 1)) & 1u) ? p1 : 0.f;
-          }
-          sum0 += p0;
-          sum1 += p1;
-          pk[u] = ptx::pack_bf16x2(p0, p1);
-        }
-        ptx::tmem_st16(tS + c * 16, pk);
-      }
-      l = l * alpha + (sum0 + sum1);
+      // the O correction comes first: the first P.V MMA of this tile
+      // accumulates into O as soon as P chunk 0 is released
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         if constexpr (D >= 32) {
 #pragma unroll
@@ -345,9 +372,30 @@ __global__ void __launch_bounds__(320, 1)
           ptx::tmem_st16(tO, o);
         }
       }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bar_pfull[t]);
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * u]), scale_log2, -mo));
+          const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * u + 1]), scale_log2, -mo));
+          sum0 += p0;
+          sum1 += p1;
+          pk[u] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st16(tS + c * 16, pk);
+        // release a chunk of P once its keys are written: every lane's
+        // stores are complete, then one lane per warp arrives (count 4)
+        constexpr int PER = 4 / C::P_CHUNKS;  // 32-key pieces per chunk
+        if ((c + 1) % PER == 0) {
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bar_pfull[t * C::P_CHUNKS + c / PER]);
+        }
+      }
+      l = l * alpha + (sum0 + sum1);
     }
 
     // ---- epilogue: O = O / l in bf16, L = m + ln l
@@ -395,12 +443,8 @@ __global__ void __launch_bounds__(320, 1)
       if (row_ok)
         LSE[static_cast<size_t>(bh) * T + grow] = (m_ref + log2f(l)) * 0.6931471805599453f;
     }
+    teardown();
   }
-
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == 0) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int D, bool CAUSAL>
@@ -413,6 +457,12 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e);
+    // the register split must fit the launch allocation, else setmaxnreg.inc
+    // would wait forever: refuse to launch instead
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, kern);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (C::REGS_SPLIT > C::THREADS * fattr.numRegs) return FA_ERR_UNSUPPORTED;
     attr_done = true;
   }
   CUtensorMap mq, mk, mv;
@@ -427,7 +477,11 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
                           Tile::TMA_SWIZZLE)) != CUDA_SUCCESS)
     return cu_status(r);
   const long long units = static_cast<long long>(a.B) * a.Hq * ((a.T + 255) / 256);
-  const float scale_log2 = a.scale * 1.4426950408889634f;
+  // scale * log2(e); never exactly 0, so that masked (infinite) scores give
+  // exponents of -inf rather than NaN: for scale = 0 the smallest normal
+  // float stands in, and every finite score's exponent still rounds to 0
+  float scale_log2 = a.scale * 1.4426950408889634f;
+  if (scale_log2 == 0.f) scale_log2 = 1.17549435e-38f;
   kern<<<static_cast<unsigned>(units), C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2);
   return cuda_status(cudaGetLastError());

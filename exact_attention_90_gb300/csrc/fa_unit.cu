@@ -245,6 +245,23 @@ __global__ void __launch_bounds__(128)
   if (warp == 0) ptx::tmem_dealloc(tmem, 256);
 }
 
+// A wait that can never complete: nothing arrives on the barrier.  Every
+// thread must give up after `budget` clocks, record the timeout and exit.
+__global__ void __launch_bounds__(128) unit_timeout_kernel(long long budget, int* gave_up) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = wait_bar(&bar, 0, &abort_flag, &g_unit_err, kErrWaitSoftmax, budget);
+  // once the flag is up, a later wait returns at once
+  const bool ok2 = wait_bar(&bar, 0, &abort_flag, &g_unit_err, kErrWaitSoftmax, budget);
+  if (!ok && !ok2) atomicAdd(gave_up, 1);
+}
+
 fa_status check_unit_ptrs(int d, std::initializer_list<const void*> ptrs) {
   for (const void* p : ptrs) {
     if (!p) return FA_ERR_INVALID_ARG;
@@ -298,6 +315,11 @@ fa_status unit_pv_impl(const float* p, const void* pb, const void* v, float* o, 
   fa_status e = set_smem<D>(reinterpret_cast<const void*>(unit_pv_kernel<D>));
   if (e != FA_OK) return e;
   unit_pv_kernel<D><<<1, 128, UnitSmem<D>::BYTES, st>>>(mv, mp, p, o, mode, lbo, sbo);
+  return cuda_status(cudaGetLastError());
+}
+
+fa_status unit_timeout_impl(long long budget, int* gave_up, cudaStream_t st) {
+  unit_timeout_kernel<<<1, 128, 0, st>>>(budget, gave_up);
   return cuda_status(cudaGetLastError());
 }
 
@@ -359,6 +381,12 @@ fa_status fa_unit_pv(const float* p, const void* pb, const void* v, float* o, in
     case 64: return fa::unit_pv_impl<64>(p, pb, v, o, mode, lbo, sbo, st);
     default: return fa::unit_pv_impl<128>(p, pb, v, o, mode, lbo, sbo, st);
   }
+}
+
+fa_status fa_unit_timeout(long long budget_cycles, int* gave_up, void* stream) {
+  if (!gave_up || budget_cycles < 1 || budget_cycles > (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(gave_up) & 3u) return FA_ERR_MISALIGNED;
+  return fa::unit_timeout_impl(budget_cycles, gave_up, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -240,6 +240,20 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register reallocation (all 128 threads of the warpgroup
+// execute the same instruction).  inc waits until the CTA's pool holds enough
+// registers, so the warpgroups' shares must add up to at most the launch
+// allocation.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math
 // 2^x on the special-function unit (documented PTX instruction).
 __device__ __forceinline__ float ex2(float x) {

@@ -29,13 +29,14 @@ enum : unsigned int {
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* err, unsigned int code) {
+                                         unsigned int* err, unsigned int code,
+                                         long long budget = FA_WAIT_BUDGET_CYCLES) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   const long long t0 = clock64();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > FA_WAIT_BUDGET_CYCLES) {
+    if (clock64() - t0 > budget) {
       *abort_flag = 1;
       atomicOr(err, code);
       return false;

@@ -54,6 +54,14 @@ fa_status fa_unit_qk(const void* q, const void* k, float* s, int d, void* stream
 fa_status fa_unit_pv(const float* p, const void* pb, const void* v, float* o, int d, int mode,
                      unsigned lbo, unsigned sbo, void* stream);
 
+/* Failure-detection check: one CTA of 128 threads waits on an mbarrier that
+ * nothing ever arrives on, bounded by budget_cycles SM clocks (1 .. 2^31).
+ * Every thread must give up, set the device error word (so that
+ * fa_debug_sync_check then returns FA_ERR_TIMEOUT) and see its second wait
+ * return at once through the CTA's abort flag; each such thread adds 1 to
+ * *gave_up (a device int, 4-byte aligned).  The context stays usable. */
+fa_status fa_unit_timeout(long long budget_cycles, int* gave_up, void* stream);
+
 /* The fp32 CUDA-core attention kernel for fp32 or bf16 inputs (same
  * arguments and semantics as fa_fwd). */
 fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,

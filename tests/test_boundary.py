@@ -36,7 +36,8 @@ def declared_functions():
 def test_headers_declare_the_abi():
     names = declared_functions()
     for n in ("fa_fwd", "fa_status_string", "fa_version", "fa_debug_sync_check",
-              "fa_last_cuda_error", "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_fwd_simt"):
+              "fa_last_cuda_error", "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout",
+              "fa_fwd_simt"):
         assert n in names
 
 
@@ -119,6 +120,10 @@ def test_unit_entry_points_reject_bad_arguments(lib):
     assert fa.fa_unit_pv(0, 0, K, O, 64, mode=0, stream=0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_unit_pv(Q, 0, K, O, 64, mode=2, stream=0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_unit_pv(Q, 0, K, O, 64, lbo=8, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_timeout(1000, 0, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_timeout(0, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_timeout(1 << 40, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_timeout(1000, O + 2, stream=0) == fa.FA_ERR_MISALIGNED
 
 
 def test_tensor_api_refuses_cpu_tensors():

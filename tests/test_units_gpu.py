@@ -118,3 +118,22 @@ def test_mma_pv_tmem_a_mnmajor_b(cuda_lib, d, mode):
         err = (o.double().cpu() - ref).abs()
         assert torch.all(err <= bound), f"max err {err.max().item():.3g}"
     assert fa.fa_debug_sync_check() == 0
+
+
+def test_bounded_wait_gives_up_and_reports(cuda_lib):
+    """A wait on a barrier that nothing arrives on ends after its budget (about
+    2 ms here), the timeout is reported once through fa_debug_sync_check, and
+    the context stays usable afterwards."""
+    fa = cuda_lib
+    assert fa.fa_debug_sync_check() == 0
+    gave_up = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert fa.fa_unit_timeout(1 << 22, gave_up) == 0
+    torch.cuda.synchronize()
+    assert gave_up.item() == 128
+    assert fa.fa_debug_sync_check() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_debug_sync_check() == 0  # read-and-clear
+    q = _bf16((1, 2, 256, 64), seed=5).cuda()
+    o, lse = fa.fwd(q, q, q, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
