@@ -12,11 +12,17 @@
 // Memory Optimization Explained", section "Key Mechanisms" (tiles that stay
 // on chip, causal look-back only).
 //
-// How it runs on Blackwell.  One CTA owns 256 query rows of one (b, h) as two
-// 128-row tiles Q0, Q1 that share every K/V tile it loads.  Warp roles:
+// How it runs on Blackwell.  A work unit is 256 query rows of one (b, h), as
+// two 128-row tiles Q0, Q1 that share every K/V tile loaded for them.  The
+// grid is persistent: one CTA per SM walks the units in longest-first order,
+// dealt in zig-zag rounds (forward, then backward) so the long causal units
+// spread evenly; tensor memory and barriers are set up once, and the next
+// unit's Q load and first S MMAs overlap the previous unit's epilogue.
+// Warp roles:
 //   warps 0-3 : softmax, correction and epilogue for Q0 (one thread per row)
 //   warps 4-7 : the same for Q1
-//   warp 8    : TMA producer (Q0, Q1 once; K_j, V_j through an NS-deep ring)
+//   warp 8    : TMA producer (Q0, Q1 once; K_j and V_j through rings of
+//               NSK and NSV stages, released separately)
 //   warp 9    : MMA issuer (one thread)
 //   warps 10-11 complete the third warpgroup, whose registers setmaxnreg
 //   hands to the two softmax warpgroups
@@ -47,28 +53,42 @@ namespace fa {
 static __device__ unsigned int g_tc_err;
 
 // Tuning parameters (compile-time; defaults are the measured best):
-//   FA_TC_P_CHUNKS   -- P is released to the MMA thread in this many pieces
 //   FA_TC_REG_SPLIT  -- 1: 384 threads, setmaxnreg moves registers from the
 //                       load/MMA warpgroup to the softmax warpgroups;
 //                       0: 320 threads, one register budget for all warps
-#ifndef FA_TC_P_CHUNKS
-#define FA_TC_P_CHUNKS 4
-#endif
 #ifndef FA_TC_REG_SPLIT
 #define FA_TC_REG_SPLIT 1
+#endif
+//   FA_TC_K_STAGES_D128 -- depth of the K ring at d = 128 (2 or 3)
+#ifndef FA_TC_K_STAGES_D128
+#define FA_TC_K_STAGES_D128 2
+#endif
+//   FA_TC_ZIGZAG -- 1: units dealt forward on even rounds, backward on odd
+//                   ones; 0: plain round robin
+#ifndef FA_TC_ZIGZAG
+#define FA_TC_ZIGZAG 1
+#endif
+//   FA_TC_PACKED_MATH -- 1: three-input max and paired fp32 FMA/add in the
+//                        softmax (half the instructions); 0: scalar
+#ifndef FA_TC_PACKED_MATH
+#define FA_TC_PACKED_MATH 1
 #endif
 
 template <int D>
 struct TcCfg : TcTile<D> {
   using Tile = TcTile<D>;
-  static constexpr int NS = D == 128 ? 2 : 4;  // K/V ring depth
+  // K and V ring depths.  K is free once both S MMAs of its tile are done,
+  // V only after both P.V MMAs, so a deeper K ring lets the next K tiles
+  // arrive early; at d = 128: Q 64 KB + K 3 x 32 KB + V 2 x 32 KB = 224 KB.
+  static constexpr int NSK = D == 128 ? FA_TC_K_STAGES_D128 : 4;
+  static constexpr int NSV = D == 128 ? 2 : 4;
   static constexpr int THREADS = FA_TC_REG_SPLIT ? 384 : 320;  // softmax Q0, Q1; load/MMA
   static constexpr int REGS_SOFTMAX = 200;  // per thread after setmaxnreg, warpgroups 0 and 1
   static constexpr int REGS_OTHER = 88;     // warpgroup 2
-  static constexpr int P_CHUNKS = FA_TC_P_CHUNKS;  // P released to the MMA in key chunks
   // registers the three warpgroups hold after reallocation
   static constexpr int REGS_SPLIT = FA_TC_REG_SPLIT ? 128 * (2 * REGS_SOFTMAX + REGS_OTHER) : 0;
-  static constexpr int SMEM_BYTES = 1024 + (2 + 2 * NS) * Tile::TILE_BYTES + 512;
+  static constexpr int SMEM_BYTES = 1024 + (2 + NSK + NSV) * Tile::TILE_BYTES + 512;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
 };
@@ -76,66 +96,104 @@ struct TcCfg : TcTile<D> {
 // log2 headroom of the lazy rescale: P values stay below 2^8
 #define FA_RESCALE_THRESHOLD 8.0f
 
+// One work unit: 256 query rows [q0, q0 + 256) of (b, h) as two 128-row
+// tiles; n0, n1 = KV tiles each tile visits (0 for a tile past T).
+struct TcUnit {
+  int bh, b, hk, q0, n0, n1, nkv;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T) {
+  TcUnit u;
+  const int BH = B * Hq;
+  const int n_qb = (T + 255) >> 8;
+  const int qb = n_qb - 1 - idx / BH;  // last (longest when causal) row blocks first
+  u.bh = idx % BH;
+  u.b = u.bh / Hq;
+  const int h = u.bh - u.b * Hq;
+  u.hk = h / (Hq / Hkv);
+  u.q0 = qb * 256;
+  const int n_all = (T + 127) >> 7;
+  const int qs1 = u.q0 + 128;
+  u.n0 = CAUSAL ? min(n_all, (u.q0 >> 7) + 1) : n_all;
+  u.n1 = qs1 >= T ? 0 : (CAUSAL ? min(n_all, (qs1 >> 7) + 1) : n_all);
+  u.nkv = max(u.n0, u.n1);
+  return u;
+}
+
+// The k-th unit of this CTA: rounds of gridDim.x units, dealt forward on even
+// rounds and backward on odd ones.
+__device__ __forceinline__ int tc_unit_index(int k) {
+  const int G = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
+  return k * G + ((FA_TC_ZIGZAG && (k & 1)) ? G - 1 - bid : bid);
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                     float* __restrict__ LSE, int B, int Hq, int Hkv, int T, float scale_log2) {
+                     float* __restrict__ LSE, int B, int Hq, int Hkv, int T, float scale_log2,
+                     int num_units) {
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
-  constexpr int NS = C::NS;
+  constexpr int NSK = C::NSK, NSV = C::NSV;
   constexpr int TILE = Tile::TILE_BYTES;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = sm;                  // Q0, Q1
-  uint8_t* sK = sm + 2 * TILE;       // NS K tiles
-  uint8_t* sV = sK + NS * TILE;      // NS V tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * TILE);
-  uint64_t* bar_q = bars;
-  uint64_t* bar_kfull = bars + 1;
-  uint64_t* bar_vfull = bar_kfull + NS;
-  uint64_t* bar_kvempty = bar_vfull + NS;
-  uint64_t* bar_sfull = bar_kvempty + NS;  // [2]
-  uint64_t* bar_pfull = bar_sfull + 2;     // [2][P_CHUNKS]
-  uint64_t* bar_odone = bar_pfull + 2 * C::P_CHUNKS;  // [2]
-  uint64_t* bar_final = bar_odone + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Shared-memory carve-up, recomputed where it is used: values computed
+  // before the per-warpgroup register reallocation would have to survive
+  // it (ptxas spills them), while these few integer operations are free.
+  struct Smem {
+    uint8_t *sQ, *sK, *sV;
+    uint64_t *qfull, *qempty, *kfull, *vfull, *kempty, *vempty, *sfull, *pfull, *odone, *final_;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    __device__ __forceinline__ explicit Smem(uint8_t* raw) {
+      uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+      sQ = sm;                  // Q0, Q1
+      sK = sm + 2 * TILE;       // NSK K tiles
+      sV = sK + NSK * TILE;     // NSV V tiles
+      uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NSV * TILE);
+      qfull = bars;             // Q0, Q1 of a unit loaded
+      qempty = bars + 1;        // the unit's last S MMA is done
+      kfull = bars + 2;
+      vfull = kfull + NSK;
+      kempty = vfull + NSV;     // K stage free: its last S MMA is done
+      vempty = kempty + NSK;    // V stage free: its last P.V MMA is done
+      sfull = vempty + NSV;     // [2]
+      pfull = sfull + 2;        // [2]
+      odone = pfull + 2;        // [2]
+      final_ = odone + 2;
+      tmem_slot = reinterpret_cast<uint32_t*>(final_ + 1);
+      abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    }
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: 256 query rows of one (b, h); longest (last) blocks first
-  const int BH = B * Hq;
-  const int n_qb = (T + 255) >> 8;
-  const int qb = n_qb - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int b = bh / Hq;
-  const int h = bh - b * Hq;
-  const int hk = h / (Hq / Hkv);
-  const int q0 = qb * 256;
-  const int n_kv_all = (T + 127) >> 7;
-  // KV tiles each Q tile visits (0 if the tile lies past T)
-  auto n_of = [&](int t) {
-    const int qs = q0 + 128 * t;
-    return qs >= T ? 0 : (CAUSAL ? min(n_kv_all, (qs >> 7) + 1) : n_kv_all);
-  };
-  const int n_t0 = n_of(0), n_t1 = n_of(1);
-  const int n_kv = max(n_t0, n_t1);
-
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar_q, 1);
-    for (int s = 0; s < NS; ++s) {
+    const Smem m(smem_raw);
+    uint64_t *bar_qfull = m.qfull, *bar_qempty = m.qempty, *bar_kfull = m.kfull,
+             *bar_kempty = m.kempty, *bar_vfull = m.vfull, *bar_vempty = m.vempty,
+             *bar_sfull = m.sfull, *bar_pfull = m.pfull, *bar_odone = m.odone,
+             *bar_final = m.final_;
+    volatile int* abort_flag = m.abort_flag;
+    ptx::mbar_init(bar_qfull, 1);
+    ptx::mbar_init(bar_qempty, 1);
+    for (int s = 0; s < NSK; ++s) {
       ptx::mbar_init(&bar_kfull[s], 1);
+      ptx::mbar_init(&bar_kempty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       ptx::mbar_init(&bar_vfull[s], 1);
-      ptx::mbar_init(&bar_kvempty[s], 1);
+      ptx::mbar_init(&bar_vempty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bar_sfull[t], 1);
-      for (int c = 0; c < C::P_CHUNKS; ++c) ptx::mbar_init(&bar_pfull[t * C::P_CHUNKS + c], 4);
+      ptx::mbar_init(&bar_pfull[t], 4);  // one elected lane per softmax warp
       ptx::mbar_init(&bar_odone[t], 1);
     }
     ptx::mbar_init(bar_final, 1);
@@ -143,17 +201,16 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_alloc(Smem(smem_raw).tmem_slot, C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   // every role ends here: all tensor-memory traffic is done before warp 0
   // frees the columns
-  auto teardown = [&]() {
+  auto teardown = [&](uint32_t tmem) {
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -165,248 +222,303 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
   if (warp >= 8) {
     // ================================================ warpgroup 2: load, MMA
     if constexpr (FA_TC_REG_SPLIT) ptx::setmaxnreg_dec<C::REGS_OTHER>();
+    const Smem m(smem_raw);
+    uint8_t *sQ = m.sQ, *sK = m.sK, *sV = m.sV;
+    uint64_t *bar_qfull = m.qfull, *bar_qempty = m.qempty, *bar_kfull = m.kfull,
+             *bar_kempty = m.kempty, *bar_vfull = m.vfull, *bar_vempty = m.vempty,
+             *bar_sfull = m.sfull, *bar_pfull = m.pfull, *bar_odone = m.odone,
+             *bar_final = m.final_;
+    volatile int* abort_flag = m.abort_flag;
+    const uint32_t tmem = *m.tmem_slot;
     if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tmQ);
-      ptx::prefetch_tmap(&tmK);
-      ptx::prefetch_tmap(&tmV);
-      const uint64_t pol_kv = ptx::policy_evict_last();
-      const uint64_t pol_q = ptx::policy_evict_first();
-      ptx::mbar_arrive_expect_tx(bar_q, 2 * TILE);
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+        const uint64_t pol_kv = ptx::policy_evict_last();
+        const uint64_t pol_q = ptx::policy_evict_first();
+        int q_issued = 0, kc = 0, vc = 0;  // Q pairs, K tiles, V tiles loaded so far
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int idx = tc_unit_index(k);
+          if (idx >= num_units) break;
+          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T);
+          // Q of the previous unit is no longer read once its last S is done
+          if (k > 0 && !wait_bar(bar_qempty, (k - 1) & 1, abort_flag, &g_tc_err, kErrWaitLoad))
+            break;
+          ptx::mbar_arrive_expect_tx(bar_qfull, 2 * TILE);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int bx = 0; bx < Tile::NBOX; ++bx)
-          ptx::tma_load_3d_hint(sQ + t * TILE + bx * Tile::BOX_BYTES, &tmQ, bar_q, bx * 64,
-                                q0 + 128 * t, bh, pol_q);
-      const int zkv = b * Hkv + hk;
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % NS;
-        if (j >= NS &&
-            !wait_bar(&bar_kvempty[st], ((j / NS) - 1) & 1, abort_flag, &g_tc_err, kErrWaitLoad))
-          break;
-        ptx::mbar_arrive_expect_tx(&bar_kfull[st], TILE);
-#pragma unroll
-        for (int bx = 0; bx < Tile::NBOX; ++bx)
-          ptx::tma_load_3d_hint(sK + st * TILE + bx * Tile::BOX_BYTES, &tmK, &bar_kfull[st],
-                                bx * 64, j * 128, zkv, pol_kv);
-        ptx::mbar_arrive_expect_tx(&bar_vfull[st], TILE);
-#pragma unroll
-        for (int bx = 0; bx < Tile::NBOX; ++bx)
-          ptx::tma_load_3d_hint(sV + st * TILE + bx * Tile::BOX_BYTES, &tmV, &bar_vfull[st],
-                                bx * 64, j * 128, zkv, pol_kv);
-        issued = j + 1;
-      }
-      // own copies still in flight (only after an abort) land before exit
-      drain_bar(bar_q, 0, &g_tc_err);
-      for (int j = max(0, issued - NS); j < issued; ++j) {
-        drain_bar(&bar_kfull[j % NS], (j / NS) & 1, &g_tc_err);
-        drain_bar(&bar_vfull[j % NS], (j / NS) & 1, &g_tc_err);
-      }
-    }
-    __syncwarp();
-    } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, D, false, true);
-      const uint32_t aQ = ptx::smem_u32(sQ);
-      const uint32_t aK = ptx::smem_u32(sK);
-      const uint32_t aV = ptx::smem_u32(sV);
-      bool ok = wait_bar(bar_q, 0, abort_flag, &g_tc_err, kErrWaitMma);
-      ptx::tc_fence_after();
-
-      // on an abort no further MMA is issued; those in flight are drained below
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j % NS;
-        if (!wait_bar(&bar_kfull[st], (j / NS) & 1, abort_flag, &g_tc_err, kErrWaitMma))
-          return false;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
-          ptx::mma_ss(tmem + C::COL_S0 + t * 128, Tile::kmajor_desc(aQ + t * TILE, kk),
-                      Tile::kmajor_desc(aK + st * TILE, kk), IDESC_QK, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(&bar_sfull[t]);
-        return true;
-      };
-
-      if (ok && n_t0 > 0) ok = issue_s(0, 0);
-      if (ok && n_t1 > 0) ok = issue_s(1, 0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % NS;
-        if (!wait_bar(&bar_vfull[st], (j / NS) & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
-          const int nt = t == 0 ? n_t0 : n_t1;
-          if (ok && j < nt) {
-            // P arrives in chunks of 32 keys (two k-steps each): the tensor
-            // core starts on the first chunk while the rest is computed
-#pragma unroll
-            for (int c = 0; c < C::P_CHUNKS; ++c) {
-              if (!wait_bar(&bar_pfull[t * C::P_CHUNKS + c], j & 1, abort_flag, &g_tc_err,
-                            kErrWaitMma)) {
-                ok = false;
-                break;
-              }
-              ptx::tc_fence_after();
-              constexpr int KPC = Tile::PV_KSTEPS / C::P_CHUNKS;
-#pragma unroll
-              for (int kq = 0; kq < KPC; ++kq) {
-                const int kk = c * KPC + kq;
-                ptx::mma_ts(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
-                            Tile::mnmajor_desc(aV + st * TILE, kk), IDESC_PV,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-              }
+            for (int bx = 0; bx < Tile::NBOX; ++bx)
+              ptx::tma_load_3d_hint(sQ + t * TILE + bx * Tile::BOX_BYTES, &tmQ, bar_qfull, bx * 64,
+                                    u.q0 + 128 * t, u.bh, pol_q);
+          q_issued = k + 1;
+          const int zkv = u.b * Hkv + u.hk;
+          for (int j = 0; j < u.nkv; ++j) {
+            const int sk = kc % NSK, sv = vc % NSV;
+            if (kc >= NSK && !wait_bar(&bar_kempty[sk], ((kc / NSK) - 1) & 1, abort_flag,
+                                       &g_tc_err, kErrWaitLoad)) {
+              ok = false;
+              break;
             }
-            if (!ok) break;
-            ptx::mma_commit(&bar_odone[t]);
-            const bool last_pv = (t == 1) || !(j < n_t1);
-            if (last_pv) ptx::mma_commit(&bar_kvempty[st]);
-            if (j + 1 < nt) ok = issue_s(t, j + 1);
+            ptx::mbar_arrive_expect_tx(&bar_kfull[sk], TILE);
+#pragma unroll
+            for (int bx = 0; bx < Tile::NBOX; ++bx)
+              ptx::tma_load_3d_hint(sK + sk * TILE + bx * Tile::BOX_BYTES, &tmK, &bar_kfull[sk],
+                                    bx * 64, j * 128, zkv, pol_kv);
+            ++kc;
+            if (vc >= NSV && !wait_bar(&bar_vempty[sv], ((vc / NSV) - 1) & 1, abort_flag,
+                                       &g_tc_err, kErrWaitLoad)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&bar_vfull[sv], TILE);
+#pragma unroll
+            for (int bx = 0; bx < Tile::NBOX; ++bx)
+              ptx::tma_load_3d_hint(sV + sv * TILE + bx * Tile::BOX_BYTES, &tmV, &bar_vfull[sv],
+                                    bx * 64, j * 128, zkv, pol_kv);
+            ++vc;
           }
         }
+        // own copies still in flight (only after an abort) land before exit
+        if (q_issued > 0) drain_bar(bar_qfull, (q_issued - 1) & 1, &g_tc_err);
+        for (int c = max(0, kc - NSK); c < kc; ++c)
+          drain_bar(&bar_kfull[c % NSK], (c / NSK) & 1, &g_tc_err);
+        for (int c = max(0, vc - NSV); c < vc; ++c)
+          drain_bar(&bar_vfull[c % NSV], (c / NSV) & 1, &g_tc_err);
       }
-      ptx::mma_commit(bar_final);
-      drain_bar(bar_final, 0, &g_tc_err);
+      __syncwarp();
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 128, false, false);
+        constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, D, false, true);
+        const uint32_t aQ = ptx::smem_u32(sQ);
+        const uint32_t aK = ptx::smem_u32(sK);
+        const uint32_t aV = ptx::smem_u32(sV);
+        int kc = 0, vc = 0;              // K, V tiles consumed so far
+        int pcnt0 = 0, pcnt1 = 0;        // P tiles consumed so far, per Q tile
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int idx = tc_unit_index(k);
+          if (idx >= num_units) break;
+          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T);
+          if (!wait_bar(bar_qfull, k & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
+          ptx::tc_fence_after();
+
+          // S_t = Q_t K_j^T; on an abort no further MMA is issued (the ones in
+          // flight are drained below)
+          auto issue_s = [&](int t, int j) -> bool {
+            const int c = kc + j;
+            const int st = c % NSK;
+            if (!wait_bar(&bar_kfull[st], (c / NSK) & 1, abort_flag, &g_tc_err, kErrWaitMma))
+              return false;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
+              ptx::mma_ss(tmem + C::COL_S0 + t * 128, Tile::kmajor_desc(aQ + t * TILE, kk),
+                          Tile::kmajor_desc(aK + st * TILE, kk), IDESC_QK, kk > 0 ? 1u : 0u);
+            ptx::mma_commit(&bar_sfull[t]);
+            // the last S of KV tile j releases its K stage (tile 1 is last when
+            // active); the unit's last S releases Q
+            if (t == 1 || j >= u.n1) ptx::mma_commit(&bar_kempty[st]);
+            if (j == u.nkv - 1 && (t == 1 || u.n1 < u.nkv)) ptx::mma_commit(bar_qempty);
+            return true;
+          };
+
+          if (ok && u.n0 > 0) ok = issue_s(0, 0);
+          if (ok && u.n1 > 0) ok = issue_s(1, 0);
+          for (int j = 0; ok && j < u.nkv; ++j) {
+            const int c = vc + j;
+            const int sv = c % NSV;
+            if (!wait_bar(&bar_vfull[sv], (c / NSV) & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int nt = t == 0 ? u.n0 : u.n1;
+              if (ok && j < nt) {
+                int& pc = t == 0 ? pcnt0 : pcnt1;
+                if (!wait_bar(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
+                  ok = false;
+                  break;
+                }
+                ++pc;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
+                  ptx::mma_ts(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
+                              Tile::mnmajor_desc(aV + sv * TILE, kk), IDESC_PV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(&bar_odone[t]);
+                const bool last_pv = (t == 1) || !(j < u.n1);
+                if (last_pv) ptx::mma_commit(&bar_vempty[sv]);
+                if (j + 1 < nt) ok = issue_s(t, j + 1);
+              }
+            }
+          }
+          kc += u.nkv;
+          vc += u.nkv;
+        }
+        ptx::mma_commit(bar_final);
+        drain_bar(bar_final, 0, &g_tc_err);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-    }
-    teardown();
+    teardown(tmem);
   } else {
     // ================================================ warpgroups 0, 1: softmax
     if constexpr (FA_TC_REG_SPLIT) ptx::setmaxnreg_inc<C::REGS_SOFTMAX>();
+    const Smem m(smem_raw);
+    uint64_t *bar_sfull = m.sfull, *bar_pfull = m.pfull, *bar_odone = m.odone;
+    volatile int* abort_flag = m.abort_flag;
+    const uint32_t tmem = *m.tmem_slot;
     const int t = warp >> 2;
     const int qr = warp & 3;
     const int row = qr * 32 + lane;
-    const int q_start = q0 + 128 * t;
-    const int grow = q_start + row;
     const uint32_t lane_off = static_cast<uint32_t>(qr * 32) << 16;
     const uint32_t tS = tmem + C::COL_S0 + t * 128 + lane_off;
     const uint32_t tO = tmem + C::COL_O0 + t * 128 + lane_off;
-    const int n = t == 0 ? n_t0 : n_t1;
     const bool neg = scale_log2 < 0.f;
     const float mask_val = neg ? INFINITY : -INFINITY;
-    float m_ref = -INFINITY;
-    float l = 0.f;
-
+    int it = 0;  // S tiles of this Q tile processed so far (barrier phases)
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      // warp-uniform decision: the tcgen05.ld/st below are warp-collective
-      ok = __all_sync(0xffffffffu,
-                      wait_bar(&bar_sfull[t], j & 1, abort_flag, &g_tc_err, kErrWaitSoftmax));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s[c]);
-      ptx::tmem_ld_wait(s[0]);
-      ptx::reg_fence(s[1]);
-      ptx::reg_fence(s[2]);
-      ptx::reg_fence(s[3]);
 
-      // masked scores become -inf (+inf when scale < 0), so that their
-      // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is never
-      // 0: the host passes the smallest normal float for scale = 0)
-      const int kb = j * 128;
-      const bool masked = (kb + 127 >= T) || (CAUSAL && kb + 127 > q_start);
-      if (masked) {
-        const int lim = CAUSAL ? min(T - 1, grow) - kb : T - 1 - kb;  // last kept column
+    for (int k = 0; ok; ++k) {
+      const int idx = tc_unit_index(k);
+      if (idx >= num_units) break;
+      const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T);
+      const int n = t == 0 ? u.n0 : u.n1;
+      const int q_start = u.q0 + 128 * t;
+      const int grow = q_start + row;
+      float m_ref = -INFINITY;
+      float l = 0.f;
+
+      for (int j = 0; j < n; ++j, ++it) {
+        // warp-uniform decision: the tcgen05.ld/st below are warp-collective
+        ok = __all_sync(0xffffffffu,
+                        wait_bar(&bar_sfull[t], it & 1, abort_flag, &g_tc_err, kErrWaitSoftmax));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t s[4][32];
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) s[c >> 5][c & 31] = __float_as_uint(mask_val);
-      }
-      float mx;
-      if (!neg) {
-        float a0 = __uint_as_float(s[0][0]), a1 = __uint_as_float(s[1][0]);
-        float a2 = __uint_as_float(s[2][0]), a3 = __uint_as_float(s[3][0]);
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s[c]);
+        ptx::tmem_ld_wait(s[0]);
+        ptx::reg_fence(s[1]);
+        ptx::reg_fence(s[2]);
+        ptx::reg_fence(s[3]);
+
+        // masked scores become -inf (+inf when scale < 0), so that their
+        // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
+        // never 0: the host passes the smallest normal float for scale = 0)
+        const int kb = j * 128;
+        const bool masked = (kb + 127 >= T) || (CAUSAL && kb + 127 > q_start);
+        if (masked) {
+          const int lim = CAUSAL ? min(T - 1, grow) - kb : T - 1 - kb;  // last kept column
 #pragma unroll
-        for (int c = 1; c < 32; ++c) {
-          a0 = fmaxf(a0, __uint_as_float(s[0][c]));
-          a1 = fmaxf(a1, __uint_as_float(s[1][c]));
-          a2 = fmaxf(a2, __uint_as_float(s[2][c]));
-          a3 = fmaxf(a3, __uint_as_float(s[3][c]));
+          for (int c = 0; c < 128; ++c)
+            if (c > lim) s[c >> 5][c & 31] = __float_as_uint(mask_val);
         }
-        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-      } else {
-        float a0 = __uint_as_float(s[0][0]), a1 = __uint_as_float(s[1][0]);
-        float a2 = __uint_as_float(s[2][0]), a3 = __uint_as_float(s[3][0]);
+        // row maximum (minimum when scale < 0) with four independent chains
+        float a[4];
 #pragma unroll
-        for (int c = 1; c < 32; ++c) {
-          a0 = fminf(a0, __uint_as_float(s[0][c]));
-          a1 = fminf(a1, __uint_as_float(s[1][c]));
-          a2 = fminf(a2, __uint_as_float(s[2][c]));
-          a3 = fminf(a3, __uint_as_float(s[3][c]));
+        for (int c = 0; c < 4; ++c) {
+          a[c] = __uint_as_float(s[c][0]);
+#pragma unroll
+          for (int v = 1; v < 31; v += 2) {
+            const float x = __uint_as_float(s[c][v]), y = __uint_as_float(s[c][v + 1]);
+            a[c] = neg ? ptx::min3(a[c], x, y) : ptx::max3(a[c], x, y);
+          }
         }
-        mx = fminf(fminf(a0, a1), fminf(a2, a3));
-      }
-      const float m_cand = mx * scale_log2;
-      const bool resc = m_cand > m_ref + FA_RESCALE_THRESHOLD;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ptx::ex2(m_ref - m_cand);  // 0 on the first tile (m_ref = -inf)
-        m_ref = m_cand;
-      }
-      const float mo = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // the O correction comes first: the first P.V MMA of this tile
-      // accumulates into O as soon as P chunk 0 is released
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        if constexpr (D >= 32) {
+        float mx;
+        if (!neg)
+          mx = ptx::max3(ptx::max3(a[0], a[1], __uint_as_float(s[0][31])),
+                         ptx::max3(a[2], a[3], __uint_as_float(s[1][31])),
+                         fmaxf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31])));
+        else
+          mx = ptx::min3(ptx::min3(a[0], a[1], __uint_as_float(s[0][31])),
+                         ptx::min3(a[2], a[3], __uint_as_float(s[1][31])),
+                         fminf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31])));
+        const float m_cand = mx * scale_log2;
+        const bool resc = m_cand > m_ref + FA_RESCALE_THRESHOLD;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ptx::ex2(m_ref - m_cand);  // 0 on the first tile (m_ref = -inf)
+          m_ref = m_cand;
+        }
+        const float mo = (m_ref == -INFINITY) ? 0.f : m_ref;
+
+        // P = 2^(s * scale_log2 - m) for two keys at a time (paired FMA),
+        // rounded to bf16 pairs into the first 64 columns of S; l sums the
+        // unrounded values
+        const uint64_t sl2x2 = ptx::f2_pack(scale_log2, scale_log2);
+        const uint64_t nmox2 = ptx::f2_pack(-mo, -mo);
+        uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
 #pragma unroll
-          for (int oc = 0; oc < D / 32; ++oc) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + oc * 32, o);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            const uint64_t x2 = ptx::fma2(
+                ptx::f2_pack(__uint_as_float(s[c][2 * v]), __uint_as_float(s[c][2 * v + 1])),
+                sl2x2, nmox2);
+            float x0, x1;
+            ptx::f2_unpack(x2, x0, x1);
+            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+            acc2[v & 1] = ptx::add2(acc2[v & 1], ptx::f2_pack(p0, p1));
+            pk[v] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st16(tS + c * 16, pk);
+        }
+        // O correction (lazy, warp-uniform), before P is released: the next
+        // P.V MMA accumulates into O
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          if constexpr (D >= 32) {
+#pragma unroll
+            for (int oc = 0; oc < D / 32; ++oc) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tO + oc * 32, o);
+              ptx::tmem_ld_wait(o);
+#pragma unroll
+              for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
+              ptx::tmem_st32(tO + oc * 32, o);
+            }
+          } else {
+            uint32_t o[16];
+            ptx::tmem_ld16(tO, o);
             ptx::tmem_ld_wait(o);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-            ptx::tmem_st32(tO + oc * 32, o);
+            for (int v = 0; v < 16; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
+            ptx::tmem_st16(tO, o);
           }
-        } else {
-          uint32_t o[16];
-          ptx::tmem_ld16(tO, o);
-          ptx::tmem_ld_wait(o);
-#pragma unroll
-          for (int u = 0; u < 16; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-          ptx::tmem_st16(tO, o);
+        }
+        // release P: every lane's stores are complete, then one lane per warp
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bar_pfull[t]);
+        {
+          const uint64_t t2 = ptx::add2(acc2[0], acc2[1]);
+          float h0, h1;
+          ptx::f2_unpack(t2, h0, h1);
+          l = l * alpha + (h0 + h1);
         }
       }
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * u]), scale_log2, -mo));
-          const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * u + 1]), scale_log2, -mo));
-          sum0 += p0;
-          sum1 += p1;
-          pk[u] = ptx::pack_bf16x2(p0, p1);
-        }
-        ptx::tmem_st16(tS + c * 16, pk);
-        // release a chunk of P once its keys are written: every lane's
-        // stores are complete, then one lane per warp arrives (count 4)
-        constexpr int PER = 4 / C::P_CHUNKS;  // 32-key pieces per chunk
-        if ((c + 1) % PER == 0) {
-          ptx::tmem_st_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bar_pfull[t * C::P_CHUNKS + c / PER]);
-        }
-      }
-      l = l * alpha + (sum0 + sum1);
-    }
+      if (!ok || n == 0) continue;
 
-    // ---- epilogue: O = O / l in bf16, L = m + ln l
-    if (ok && n > 0)
-      ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (n - 1) & 1, abort_flag, &g_tc_err,
+      // ---- epilogue: O = O / l in bf16, L = m + ln l (the tensor core meanwhile
+      // computes the next unit's first S tiles)
+      ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (it - 1) & 1, abort_flag, &g_tc_err,
                                             kErrWaitEpilogue));
-    if (ok && n > 0) {
+      if (!ok) break;
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = grow < T;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * T + (row_ok ? grow : 0)) * D;
+      __nv_bfloat16* orow = O + (static_cast<size_t>(u.bh) * T + (row_ok ? grow : 0)) * D;
       if constexpr (D >= 32) {
 #pragma unroll
         for (int oc = 0; oc < D / 32; ++oc) {
@@ -415,9 +527,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
           ptx::tmem_ld_wait(o);
           uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            pk[u] = ptx::pack_bf16x2(__uint_as_float(o[2 * u]) * inv_l,
-                                     __uint_as_float(o[2 * u + 1]) * inv_l);
+          for (int v = 0; v < 16; ++v)
+            pk[v] = ptx::pack_bf16x2(__uint_as_float(o[2 * v]) * inv_l,
+                                     __uint_as_float(o[2 * v + 1]) * inv_l);
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(orow + oc * 32);
 #pragma unroll
@@ -431,9 +543,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         ptx::tmem_ld_wait(o);
         uint32_t pk[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          pk[u] = ptx::pack_bf16x2(__uint_as_float(o[2 * u]) * inv_l,
-                                   __uint_as_float(o[2 * u + 1]) * inv_l);
+        for (int v = 0; v < 8; ++v)
+          pk[v] = ptx::pack_bf16x2(__uint_as_float(o[2 * v]) * inv_l,
+                                   __uint_as_float(o[2 * v + 1]) * inv_l);
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow);
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -441,10 +553,26 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         }
       }
       if (row_ok)
-        LSE[static_cast<size_t>(bh) * T + grow] = (m_ref + log2f(l)) * 0.6931471805599453f;
+        LSE[static_cast<size_t>(u.bh) * T + grow] = (m_ref + log2f(l)) * 0.6931471805599453f;
+      // the O reads above are complete before this warp releases its next P
+      ptx::tc_fence_before();
     }
-    teardown();
+    teardown(tmem);
   }
+}
+
+// SMs of the current device (cached per device)
+static int tc_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
 }
 
 template <int D, bool CAUSAL>
@@ -477,13 +605,15 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
                           Tile::TMA_SWIZZLE)) != CUDA_SUCCESS)
     return cu_status(r);
   const long long units = static_cast<long long>(a.B) * a.Hq * ((a.T + 255) / 256);
+  const long long grid = units < tc_sm_count() ? units : tc_sm_count();  // one CTA per SM
   // scale * log2(e); never exactly 0, so that masked (infinite) scores give
   // exponents of -inf rather than NaN: for scale = 0 the smallest normal
   // float stands in, and every finite score's exponent still rounds to 0
   float scale_log2 = a.scale * 1.4426950408889634f;
   if (scale_log2 == 0.f) scale_log2 = 1.17549435e-38f;
-  kern<<<static_cast<unsigned>(units), C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
+      static_cast<int>(units));
   return cuda_status(cudaGetLastError());
 }
 
