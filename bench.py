@@ -306,7 +306,8 @@ def run_ours(args, w):
         if flush is not None:
             flush.zero_()
         st = fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.T, w.d, w.scale, int(w.causal),
-                       fa.FA_DTYPE_BF16 if w.dtype == "bf16" else fa.FA_DTYPE_F32, stream)
+                       {"bf16": fa.FA_DTYPE_BF16, "f16": fa.FA_DTYPE_F16,
+                        "f32": fa.FA_DTYPE_F32}[w.dtype], stream)
         if st != 0:
             raise fa.FaError(st, "fa_fwd")
 
@@ -381,7 +382,9 @@ def run_ours(args, w):
     peaks, src = load_peaks()
     ms_per = ms / args.steps
     achieved = w.flops / (ms_per / 1e3) / 1e12
-    peak = float(peaks["bf16_tflops"]) if w.dtype == "bf16" else None
+    # fp16 and bf16 share the dense tensor rate (nominal ratio 1:1); the fp32
+    # kernel runs on the CUDA cores and has no tensor peak
+    peak = float(peaks["bf16_tflops"]) if w.dtype in ("bf16", "f16") else None
     traffic = ncu_traffic(w.name)
     clocks = sampler.summary(t_wall0, t_wall1)
 
@@ -401,7 +404,7 @@ def run_ours(args, w):
                      "algorithmic_bytes_per_launch": w.bytes,
                      "hbm_gbs": w.bytes / (ms_per / 1e3) / 1e9,
                      "hbm_frac": w.bytes / (ms_per / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
-                     "kernel": "fa_fwd_tc_kernel" if w.dtype == "bf16" else "fa_fwd_simt_kernel"},
+                     "kernel": "fa_fwd_simt_kernel" if w.dtype == "f32" else "fa_fwd_tc_kernel"},
         "clocks": clocks,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:

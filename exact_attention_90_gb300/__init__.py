@@ -26,7 +26,7 @@ __all__ = [
     "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
     "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "FA_DTYPE_F32",
-    "FA_DTYPE_BF16",
+    "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
 
 FA_OK = 0
@@ -37,6 +37,7 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_DTYPE_F32 = 0
 FA_DTYPE_BF16 = 1
+FA_DTYPE_F16 = 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -171,9 +172,11 @@ def _dtype_code(t) -> int:
 
     if t.dtype == torch.bfloat16:
         return FA_DTYPE_BF16
+    if t.dtype == torch.float16:
+        return FA_DTYPE_F16
     if t.dtype == torch.float32:
         return FA_DTYPE_F32
-    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16, float16 or float32)")
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
@@ -181,7 +184,7 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     """Attention forward on CUDA tensors; returns (o, lse).
 
     q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; all contiguous CUDA tensors of one
-    dtype (bfloat16 or float32).  scale defaults to 1/sqrt(d).  ``out`` and
+    dtype (bfloat16, float16 or float32).  scale defaults to 1/sqrt(d).  ``out`` and
     ``lse`` may be given (shapes [B,Hq,T,d] in the input dtype and [B,Hq,T]
     float32); otherwise they are allocated with torch.  ``kernel="simt"``
     forces the fp32 CUDA-core kernel (also for bf16 inputs); the default picks

@@ -44,7 +44,8 @@ fa_status validate_fwd(const FwdArgs& a) {
   if (a.Hq % a.Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.causal != 0 && a.causal != 1) return FA_ERR_INVALID_ARG;
-  if (a.dtype != FA_DTYPE_F32 && a.dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  if (a.dtype != FA_DTYPE_F32 && a.dtype != FA_DTYPE_BF16 && a.dtype != FA_DTYPE_F16)
+    return FA_ERR_UNSUPPORTED;
   if (a.d != 16 && a.d != 32 && a.d != 64 && a.d != 128) return FA_ERR_UNSUPPORTED;
   // sizes: element counts must fit comfortably in 63 bits and the grid in 2^31
   const double eq = static_cast<double>(a.B) * a.Hq * a.T * a.d;
@@ -85,8 +86,8 @@ static void load_encode() {
   g_encode_status = CUDA_SUCCESS;
 }
 
-CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long long BH, int box_x,
-                        int swizzle) {
+CUresult make_tmap_16bit(CUtensorMap* map, const void* base, int d, int T, long long BH,
+                         int box_x, int swizzle, bool f16) {
   std::call_once(g_encode_once, load_encode);
   if (g_encode_status != CUDA_SUCCESS) return g_encode_status;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
@@ -95,7 +96,8 @@ CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long l
                            static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(d) * 2};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), 128u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  return g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   static_cast<CUtensorMapSwizzle>(swizzle), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -124,7 +126,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                 static_cast<cudaStream_t>(stream)};
   fa_status s = fa::validate_fwd(a);
   if (s != FA_OK) return s;
-  return dtype == FA_DTYPE_BF16 ? fa::launch_tc(a) : fa::launch_simt(a);
+  return dtype == FA_DTYPE_F32 ? fa::launch_simt(a) : fa::launch_tc(a);
 }
 
 fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -30,14 +30,19 @@ fa_status validate_fwd(const FwdArgs& a);
 fa_status cuda_status(cudaError_t e);
 fa_status cu_status(CUresult r);
 
-// 3-D bf16 tensor map over a contiguous [BH][T][d] tensor with boxes of
-// box_x columns x 128 rows x 1 and the given swizzle (CUtensorMapSwizzle).
-CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long long BH,
-                        int box_x, int swizzle);
+// 3-D tensor map over a contiguous [BH][T][d] tensor of 16-bit elements
+// (fp16 when f16, else bf16) with boxes of box_x columns x 128 rows x 1 and
+// the given swizzle (CUtensorMapSwizzle).
+CUresult make_tmap_16bit(CUtensorMap* map, const void* base, int d, int T, long long BH,
+                         int box_x, int swizzle, bool f16);
+inline CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long long BH,
+                               int box_x, int swizzle) {
+  return make_tmap_16bit(map, base, d, T, BH, box_x, swizzle, false);
+}
 
 // Kernel launchers (enqueue only; arguments already validated).
-fa_status launch_tc(const FwdArgs& a);    // bf16, tcgen05
-fa_status launch_simt(const FwdArgs& a);  // fp32 or bf16, CUDA cores
+fa_status launch_tc(const FwdArgs& a);    // bf16 / fp16, tcgen05
+fa_status launch_simt(const FwdArgs& a);  // fp32, bf16 or fp16, CUDA cores
 
 // Device error word shared by the kernels (read-and-clear, synchronous).
 fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word);

@@ -7,8 +7,9 @@
 // accumulator rescaled by exp(m_old - m_new) per block (section "Softmax 的在線
 // 計算"), O / l and L = m + log l at the end -- with every product done by FFMA
 // in fp32.  fp32 inputs need this path: a TF32 tensor-core product would not
-// keep O within 1e-4 of the exact result.  It also accepts bf16 inputs (fp32
-// arithmetic), which the tests use as a cross-check of the tensor-core kernel.
+// keep O within 1e-4 of the exact result.  It also accepts bf16 and fp16 inputs
+// (fp32 arithmetic), which the tests use as a cross-check of the tensor-core
+// kernel.
 //
 // CTA = 128 threads = a 16 x 8 grid (tx, ty) over a 64-query x 64-key block:
 // thread (tx, ty) owns query rows ty*8 .. ty*8+7, score columns tx*4 .. tx*4+3
@@ -20,6 +21,7 @@
 #include "fa_internal.h"
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace fa {
 
@@ -77,6 +79,40 @@ __device__ __forceinline__ void load_tile(float* dst, const __nv_bfloat16* src, 
     float* d = dst + r * LS + 8 * c8;
     *reinterpret_cast<float4*>(d) = make_float4(f[0], f[1], f[2], f[3]);
     *reinterpret_cast<float4*>(d + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+template <int D, int LS>
+__device__ __forceinline__ void load_tile(float* dst, const __half* src, int r0, int T) {
+  constexpr int V = D / 8;  // 16-byte vectors of 8 fp16 per row
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < 64 * V; idx += 128) {
+    const int r = idx / V, c8 = idx % V;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < T) x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r0 + r) * D) + c8);
+    const __half2* h = reinterpret_cast<const __half2*>(&x);
+    float* d = dst + r * LS + 8 * c8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h[e]);
+      d[2 * e] = f.x;
+      d[2 * e + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_out(__half* dst, const float* x, int n) {
+  if (n == 4) {
+    __half2 a = __floats2half2_rn(x[0], x[1]);
+    __half2 b = __floats2half2_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else if (n == 2) {
+    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(x[0], x[1]);
+  } else {
+    dst[0] = __float2half_rn(x[0]);
   }
 }
 
@@ -295,6 +331,7 @@ fa_status launch_simt_t(const FwdArgs& a) {
 fa_status launch_simt(const FwdArgs& a) {
   if (a.dtype == FA_DTYPE_F32) return launch_simt_t<float>(a);
   if (a.dtype == FA_DTYPE_BF16) return launch_simt_t<__nv_bfloat16>(a);
+  if (a.dtype == FA_DTYPE_F16) return launch_simt_t<__half>(a);
   return FA_ERR_UNSUPPORTED;
 }
 

@@ -1,4 +1,4 @@
-// fa_tc.cu -- bf16 exact attention forward on tcgen05 tensor cores (sm_103a).
+// fa_tc.cu -- bf16 / fp16 exact attention forward on tcgen05 tensor cores (sm_103a).
 //
 // What it computes: for every (batch, query head) and every query row, the
 // scaled dot-product attention output O = softmax(scale * Q K^T + mask) V and
@@ -128,11 +128,12 @@ __device__ __forceinline__ int tc_unit_index(int k) {
   return k * G + ((FA_TC_ZIGZAG && (k & 1)) ? G - 1 - bid : bid);
 }
 
-template <int D, bool CAUSAL>
+// F16: fp16 operands and output (else bf16); accumulation is fp32 either way
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                     const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
                      float* __restrict__ LSE, int B, int Hq, int Hkv, int T, float scale_log2,
                      int num_units) {
   using C = TcCfg<D>;
@@ -293,8 +294,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     } else if (warp == 9) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, 128, false, false);
-        constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, D, false, true);
+        constexpr uint32_t IDESC_QK = ptx::idesc_16bit(128, 128, false, false, F16);
+        constexpr uint32_t IDESC_PV = ptx::idesc_16bit(128, D, false, true, F16);
         const uint32_t aQ = ptx::smem_u32(sQ);
         const uint32_t aK = ptx::smem_u32(sK);
         const uint32_t aV = ptx::smem_u32(sV);
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             ptx::f2_unpack(x2, x0, x1);
             const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
             acc2[v & 1] = ptx::add2(acc2[v & 1], ptx::f2_pack(p0, p1));
-            pk[v] = ptx::pack_bf16x2(p0, p1);
+            pk[v] = ptx::pack_x2<F16>(p0, p1);
           }
           ptx::tmem_st16(tS + c * 16, pk);
         }
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = grow < T;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(u.bh) * T + (row_ok ? grow : 0)) * D;
+      uint16_t* orow = O + (static_cast<size_t>(u.bh) * T + (row_ok ? grow : 0)) * D;
       if constexpr (D >= 32) {
 #pragma unroll
         for (int oc = 0; oc < D / 32; ++oc) {
@@ -528,8 +529,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int v = 0; v < 16; ++v)
-            pk[v] = ptx::pack_bf16x2(__uint_as_float(o[2 * v]) * inv_l,
-                                     __uint_as_float(o[2 * v + 1]) * inv_l);
+            pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * inv_l,
+                                      __uint_as_float(o[2 * v + 1]) * inv_l);
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(orow + oc * 32);
 #pragma unroll
@@ -544,8 +545,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         uint32_t pk[8];
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          pk[v] = ptx::pack_bf16x2(__uint_as_float(o[2 * v]) * inv_l,
-                                   __uint_as_float(o[2 * v + 1]) * inv_l);
+          pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * inv_l,
+                                    __uint_as_float(o[2 * v + 1]) * inv_l);
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow);
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -575,11 +576,11 @@ static int tc_sm_count() {
   return cache[dev];
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 static fa_status launch_tc_impl(const FwdArgs& a) {
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
-  auto kern = fa_fwd_tc_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_tc_kernel<D, CAUSAL, F16>;
   static bool attr_done = false;  // per instantiation; benign race (idempotent)
   if (!attr_done) {
     cudaError_t e =
@@ -595,14 +596,14 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
   }
   CUtensorMap mq, mk, mv;
   CUresult r;
-  if ((r = make_tmap_bf16(&mq, a.q, D, a.T, static_cast<long long>(a.B) * a.Hq, Tile::BOX_X,
-                          Tile::TMA_SWIZZLE)) != CUDA_SUCCESS)
+  if ((r = make_tmap_16bit(&mq, a.q, D, a.T, static_cast<long long>(a.B) * a.Hq, Tile::BOX_X,
+                           Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
     return cu_status(r);
-  if ((r = make_tmap_bf16(&mk, a.k, D, a.T, static_cast<long long>(a.B) * a.Hkv, Tile::BOX_X,
-                          Tile::TMA_SWIZZLE)) != CUDA_SUCCESS)
+  if ((r = make_tmap_16bit(&mk, a.k, D, a.T, static_cast<long long>(a.B) * a.Hkv, Tile::BOX_X,
+                           Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
     return cu_status(r);
-  if ((r = make_tmap_bf16(&mv, a.v, D, a.T, static_cast<long long>(a.B) * a.Hkv, Tile::BOX_X,
-                          Tile::TMA_SWIZZLE)) != CUDA_SUCCESS)
+  if ((r = make_tmap_16bit(&mv, a.v, D, a.T, static_cast<long long>(a.B) * a.Hkv, Tile::BOX_X,
+                           Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
     return cu_status(r);
   const long long units = static_cast<long long>(a.B) * a.Hq * ((a.T + 255) / 256);
   const long long grid = units < tc_sm_count() ? units : tc_sm_count();  // one CTA per SM
@@ -612,20 +613,27 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
   float scale_log2 = a.scale * 1.4426950408889634f;
   if (scale_log2 == 0.f) scale_log2 = 1.17549435e-38f;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
+      mq, mk, mv, static_cast<uint16_t*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
       static_cast<int>(units));
   return cuda_status(cudaGetLastError());
 }
 
-fa_status launch_tc(const FwdArgs& a) {
+template <bool F16>
+static fa_status launch_tc_t(const FwdArgs& a) {
   const bool c = a.causal != 0;
   switch (a.d) {
-    case 16: return c ? launch_tc_impl<16, true>(a) : launch_tc_impl<16, false>(a);
-    case 32: return c ? launch_tc_impl<32, true>(a) : launch_tc_impl<32, false>(a);
-    case 64: return c ? launch_tc_impl<64, true>(a) : launch_tc_impl<64, false>(a);
-    case 128: return c ? launch_tc_impl<128, true>(a) : launch_tc_impl<128, false>(a);
+    case 16: return c ? launch_tc_impl<16, true, F16>(a) : launch_tc_impl<16, false, F16>(a);
+    case 32: return c ? launch_tc_impl<32, true, F16>(a) : launch_tc_impl<32, false, F16>(a);
+    case 64: return c ? launch_tc_impl<64, true, F16>(a) : launch_tc_impl<64, false, F16>(a);
+    case 128: return c ? launch_tc_impl<128, true, F16>(a) : launch_tc_impl<128, false, F16>(a);
     default: return FA_ERR_UNSUPPORTED;
   }
+}
+
+fa_status launch_tc(const FwdArgs& a) {
+  if (a.dtype == FA_DTYPE_BF16) return launch_tc_t<false>(a);
+  if (a.dtype == FA_DTYPE_F16) return launch_tc_t<true>(a);
+  return FA_ERR_UNSUPPORTED;
 }
 
 fa_status tc_read_and_clear_error(unsigned int* word) {

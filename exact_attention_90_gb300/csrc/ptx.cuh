@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace fa {
 namespace ptx {
@@ -300,6 +301,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two fp32 -> packed f16x2 (round to nearest even); `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Pair packing in the 16-bit input type of the kernel (F16: fp16, else bf16).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
+  if constexpr (F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory layout codes of the tcgen05 matrix descriptor (bits 61..63).
 enum : uint32_t { kLayoutNone = 0, kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6 };
@@ -326,15 +340,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// tcgen05 instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
-//   [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format,
-//   [15] A major (0 = K-major, 1 = MN-major), [16] B major,
+// tcgen05 instruction descriptor for kind::f16 with fp32 D and A/B both fp16
+// (f16 = true) or both bf16:
+//   [4,6) D format (1 = f32), [7,10) A format (0 = f16, 1 = bf16), [10,13) B
+//   format, [15] A major (0 = K-major, 1 = MN-major), [16] B major,
 //   [17,23) N >> 3, [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
-                                                  bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
-         (static_cast<uint32_t>(b_mn_major) << 16) |
+__host__ __device__ constexpr uint32_t idesc_16bit(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                   bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_16bit(M, N, a_mn_major, b_mn_major, false);
 }
 
 }  // namespace ptx

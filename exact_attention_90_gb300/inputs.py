@@ -12,12 +12,12 @@ from __future__ import annotations
 
 import torch
 
-DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 def make_qkv(B: int, Hq: int, Hkv: int, T: int, d: int, dtype: str = "bf16",
              seed: int = 0, mult: float = 1.0, device: str = "cpu"):
-    """Q [B,Hq,T,d], K and V [B,Hkv,T,d], contiguous, in ``dtype`` ("f32"/"bf16").
+    """Q [B,Hq,T,d], K and V [B,Hkv,T,d], contiguous, in ``dtype`` ("f32"/"bf16"/"f16").
 
     Q, K and V are drawn in that order from one generator seeded with ``seed``.
     """

@@ -21,7 +21,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass, field
 
-ELEM_BYTES = {"f32": 4, "bf16": 2}
+ELEM_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
 
 
 @dataclass(frozen=True)
@@ -32,7 +32,7 @@ class Workload:
     Hkv: int
     T: int
     d: int
-    dtype: str          # "f32" or "bf16"
+    dtype: str          # "f32", "bf16" or "f16"
     causal: bool
     scale: float
     mult: float = 1.0   # Q, K, V = N(0,1) * mult before rounding to dtype

@@ -33,9 +33,13 @@
  * that owns the buffers.
  *
  * Kernels by dtype (selection by the arithmetic type, not a fallback):
- *   FA_DTYPE_BF16: TMA-staged swizzled tiles, tcgen05 MMA into tensor memory,
- *                  warp-specialised softmax (d in {16, 32, 64, 128});
+ *   FA_DTYPE_BF16, FA_DTYPE_F16: TMA-staged swizzled tiles, tcgen05 MMA into
+ *                  tensor memory (bf16 or fp16 operands, fp32 accumulation),
+ *                  warp-specialised softmax (d in {16, 32, 64, 128}); P is
+ *                  rounded to the input type for the second product;
  *   FA_DTYPE_F32 : true-fp32 FFMA kernel on the CUDA cores (same d).
+ * The pages name FP16 and BF16 as the tensor-core precisions ("Flash
+ * Attention Memory Optimization Explained", section "Key Mechanisms"). 
  * Dropout and arbitrary attention masks are not supported.
  */
 #ifndef FA_H_
@@ -57,7 +61,7 @@ typedef enum {
                              by fa_debug_sync_check only) */
 } fa_status;
 
-typedef enum { FA_DTYPE_F32 = 0, FA_DTYPE_BF16 = 1 } fa_dtype;
+typedef enum { FA_DTYPE_F32 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_F16 = 2 } fa_dtype;
 
 /* Exact attention forward with log-sum-exp (see the header comment).
  *   q, k, v : device inputs; o, lse : device outputs

@@ -31,7 +31,7 @@ def run(fa, q, k, v, causal, scale=None, kernel="auto"):
     return o, lse
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", DS)
 @pytest.mark.parametrize("T", [1, 5, 64, 127, 129, 200, 257, 640, 1000])
@@ -42,7 +42,7 @@ def test_full_parity_ragged(cuda_lib, T, d, causal, dtype):
     check_full(o, lse, q, k, v, scale, causal, what=f"T={T} d={d} causal={causal} {dtype}")
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("Hq,Hkv", [(8, 1), (8, 2), (8, 8), (6, 3)])
 def test_full_parity_grouped_heads(cuda_lib, Hq, Hkv, dtype):
     for causal in (False, True):
@@ -51,7 +51,7 @@ def test_full_parity_grouped_heads(cuda_lib, Hq, Hkv, dtype):
         check_full(o, lse, q, k, v, 0.125, causal, what=f"Hq={Hq} Hkv={Hkv} {dtype}")
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("scale", [0.0, -0.09, 0.7])
 def test_full_parity_scale_edge_cases(cuda_lib, scale, dtype):
     for causal in (False, True):
@@ -80,7 +80,7 @@ def fp32_lse_bound(q, k, scale):
     return abs(scale) * gamma * worst
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_full_parity_growing_row_max(cuda_lib, d, dtype):
     """Row maxima that keep rising along the keys: the accumulator has to be
@@ -108,7 +108,7 @@ def test_causal_row0_and_zero_query_closed_forms(cuda_lib):
     """Closed forms on the device: causal row 0 returns V[0] (exactly, up to
     output rounding) and Q = 0 gives LSE[i] = ln(i+1)."""
     fa = cuda_lib
-    for dtype in ("bf16", "f32"):
+    for dtype in ("bf16", "f32", "f16"):
         q, k, v = make_qkv(2, 2, 2, 500, 64, dtype=dtype, seed=3, device="cuda")
         o, lse = run(fa, q, k, v, True, 0.125)
         assert torch.equal(o[:, :, 0, :], v[:, :, 0, :])
@@ -119,10 +119,11 @@ def test_causal_row0_and_zero_query_closed_forms(cuda_lib):
         assert err <= TOL[dtype][1]
 
 
-def test_bf16_tensor_core_agrees_with_fp32_simt(cuda_lib):
-    """The tcgen05 kernel and the CUDA-core kernel on the same bf16 inputs."""
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tensor_core_agrees_with_fp32_simt(cuda_lib, dtype):
+    """The tcgen05 kernel and the CUDA-core kernel on the same 16-bit inputs."""
     fa = cuda_lib
-    q, k, v = make_qkv(2, 4, 4, 777, 128, dtype="bf16", seed=9, device="cuda")
+    q, k, v = make_qkv(2, 4, 4, 777, 128, dtype=dtype, seed=9, device="cuda")
     for causal in (False, True):
         o1, l1 = run(fa, q, k, v, causal)
         o2, l2 = run(fa, q, k, v, causal, kernel="simt")
@@ -135,7 +136,7 @@ def test_deterministic_and_no_stray_writes(cuda_lib):
     (guard regions around both outputs)."""
     fa = cuda_lib
     B, H, T, d = 2, 3, 333, 128
-    for dtype in ("bf16", "f32"):
+    for dtype in ("bf16", "f32", "f16"):
         q, k, v = make_qkv(B, H, H, T, d, dtype=dtype, seed=4, device="cuda")
         tdt = q.dtype
         pad_o, pad_l = 4096, 1024
