@@ -25,7 +25,8 @@ import os
 __all__ = [
     "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
-    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "FA_DTYPE_F32",
+    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_split",
+    "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
 
@@ -35,6 +36,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_MISALIGNED = 3
 FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
+FA_ERR_WORKSPACE = 6
 FA_DTYPE_F32 = 0
 FA_DTYPE_BF16 = 1
 FA_DTYPE_F16 = 2
@@ -54,6 +56,10 @@ EXPORTS = [
     ("fa_unit_qk", _I, [_P, _P, _P, _I, _P]),
     ("fa_unit_pv", _I, [_P, _P, _P, _P, _I, _I, ctypes.c_uint, ctypes.c_uint, _P]),
     ("fa_unit_timeout", _I, [ctypes.c_longlong, _P, _P]),
+    ("fa_fwd_split", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
+                          ctypes.c_ulonglong, _P]),
+    ("fa_fwd_split_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I]),
+    ("fa_fwd_split_heuristic", _I, [_I, _I, _I, _I, _I, _I]),
     ("fa_fwd_simt", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
 ]
 
@@ -133,6 +139,26 @@ def fa_fwd_simt(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, stream=
                            _stream(stream))
 
 
+def fa_fwd_split(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, num_splits,
+                 workspace, workspace_bytes, stream=None) -> int:
+    """The C function fa_fwd_split (split-KV forward into a caller workspace)."""
+    lib = load_library()
+    return lib.fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                            int(Hkv), int(T), int(d), float(scale), int(causal), int(dtype),
+                            int(num_splits), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
+
+
+def fa_fwd_split_workspace_size(B, Hq, T, d, num_splits) -> int:
+    return load_library().fa_fwd_split_workspace_size(int(B), int(Hq), int(T), int(d),
+                                                      int(num_splits))
+
+
+def fa_fwd_split_heuristic(B, Hq, Hkv, T, d, causal) -> int:
+    return load_library().fa_fwd_split_heuristic(int(B), int(Hq), int(Hkv), int(T), int(d),
+                                                 int(causal))
+
+
 def fa_status_string(status: int) -> str:
     return load_library().fa_status_string(int(status)).decode()
 
@@ -180,16 +206,19 @@ def _dtype_code(t) -> int:
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-        stream=None, kernel: str = "auto"):
+        stream=None, kernel: str = "auto", num_splits: int | None = None):
     """Attention forward on CUDA tensors; returns (o, lse).
 
     q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; all contiguous CUDA tensors of one
     dtype (bfloat16, float16 or float32).  scale defaults to 1/sqrt(d).  ``out`` and
     ``lse`` may be given (shapes [B,Hq,T,d] in the input dtype and [B,Hq,T]
     float32); otherwise they are allocated with torch.  ``kernel="simt"``
-    forces the fp32 CUDA-core kernel (also for bf16 inputs); the default picks
-    the kernel by dtype.  The call is asynchronous on ``stream`` (default: the
-    current torch stream).
+    forces the fp32 CUDA-core kernel (also for 16-bit inputs); the default
+    picks the kernel by dtype.  ``num_splits`` splits every row block's keys
+    that many ways (16-bit inputs; None = the library's heuristic, which
+    splits only shapes too small to fill the GPU); the split path's
+    workspace is allocated with torch.  The call is asynchronous on
+    ``stream`` (default: the current torch stream).
     """
     import torch
 
@@ -211,9 +240,24 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
-    call = fa_fwd_simt if kernel == "simt" else fa_fwd
     if kernel not in ("auto", "simt"):
         raise ValueError("kernel must be 'auto' or 'simt'")
-    st = call(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code, stream)
-    _check(st, "fa_fwd")
+    if kernel == "simt":
+        st = fa_fwd_simt(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code,
+                         stream)
+        _check(st, "fa_fwd_simt")
+        return out, lse
+    splits = 1
+    if code != FA_DTYPE_F32:
+        splits = (fa_fwd_split_heuristic(B, Hq, Hkv, T, d, int(bool(causal)))
+                  if num_splits is None else int(num_splits))
+    if splits > 1:
+        nbytes = fa_fwd_split_workspace_size(B, Hq, T, d, splits)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        st = fa_fwd_split(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code,
+                          splits, ws, nbytes, stream)
+        _check(st, "fa_fwd_split")
+    else:
+        st = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code, stream)
+        _check(st, "fa_fwd")
     return out, lse

@@ -33,7 +33,7 @@ fa_status cu_status(CUresult r) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
 }
@@ -139,6 +139,43 @@ fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, floa
   return fa::launch_simt(a);
 }
 
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int T, int d, float scale, int causal, fa_dtype dtype,
+                       int num_splits, void* workspace, unsigned long long workspace_bytes,
+                       void* stream) {
+  fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype,
+                static_cast<cudaStream_t>(stream)};
+  fa_status s = fa::validate_fwd(a);
+  if (s != FA_OK) return s;
+  if (num_splits < 1 || num_splits > fa::kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F32) return fa::launch_simt(a);
+  if (num_splits == 1) return fa::launch_tc(a);
+  if (workspace == nullptr) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
+  const size_t need = fa::split_workspace_bytes(B, Hq, T, d, num_splits);
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const size_t e = 2;
+  const size_t nq = static_cast<size_t>(B) * Hq * T * d * e;
+  const size_t nkv = static_cast<size_t>(B) * Hkv * T * d * e;
+  const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+  if (fa::overlap(workspace, need, q, nq) || fa::overlap(workspace, need, k, nkv) ||
+      fa::overlap(workspace, need, v, nkv) || fa::overlap(workspace, need, o, nq) ||
+      fa::overlap(workspace, need, lse, nl))
+    return FA_ERR_INVALID_ARG;
+  return fa::launch_tc_split(a, num_splits, workspace, workspace_bytes);
+}
+
+unsigned long long fa_fwd_split_workspace_size(int B, int Hq, int T, int d, int num_splits) {
+  if (B <= 0 || Hq <= 0 || T <= 0 || d <= 0 || num_splits < 1 || num_splits > fa::kMaxSplits)
+    return 0;
+  return fa::split_workspace_bytes(B, Hq, T, d, num_splits);
+}
+
+int fa_fwd_split_heuristic(int B, int Hq, int Hkv, int T, int d, int causal) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || d <= 0) return 1;
+  return fa::split_heuristic(B, Hq, T, causal);
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "ok";
@@ -147,6 +184,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case FA_ERR_WORKSPACE: return "scratch workspace missing or too small";
     default: return "unknown status";
   }
 }

@@ -25,6 +25,7 @@ struct FwdArgs {
 
 // Host-side argument checks shared by every entry point (no CUDA calls).
 fa_status validate_fwd(const FwdArgs& a);
+bool overlap(const void* a, size_t na, const void* b, size_t nb);
 
 // Records a CUDA error for fa_last_cuda_error() and maps it to a status.
 fa_status cuda_status(cudaError_t e);
@@ -42,6 +43,13 @@ inline CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T,
 
 // Kernel launchers (enqueue only; arguments already validated).
 fa_status launch_tc(const FwdArgs& a);    // bf16 / fp16, tcgen05
+// the same with the KV range of every row block split S ways: partial
+// results go to `workspace` (split_workspace_bytes(...) bytes), a second
+// kernel merges them into o and lse
+fa_status launch_tc_split(const FwdArgs& a, int S, void* workspace, size_t workspace_bytes);
+size_t split_workspace_bytes(int B, int Hq, int T, int d, int S);
+int split_heuristic(int B, int Hq, int T, int causal);
+constexpr int kMaxSplits = 64;
 fa_status launch_simt(const FwdArgs& a);  // fp32, bf16 or fp16, CUDA cores
 
 // Device error word shared by the kernels (read-and-clear, synchronous).

@@ -96,28 +96,46 @@ struct TcCfg : TcTile<D> {
 // log2 headroom of the lazy rescale: P values stay below 2^8
 #define FA_RESCALE_THRESHOLD 8.0f
 
+// KV tiles visited by the two 128-row Q tiles of row block qb (256 rows):
+// all tiles, or when causal those up to the diagonal; 0 for a tile past T.
+__host__ __device__ __forceinline__ void tc_tile_counts(int qb, int T, bool causal, int& n0,
+                                                        int& n1) {
+  const int n_all = (T + 127) >> 7;
+  const int qs0 = qb * 256, qs1 = qs0 + 128;
+  n0 = causal ? min(n_all, (qs0 >> 7) + 1) : n_all;
+  n1 = qs1 >= T ? 0 : (causal ? min(n_all, (qs1 >> 7) + 1) : n_all);
+}
+
 // One work unit: 256 query rows [q0, q0 + 256) of (b, h) as two 128-row
-// tiles; n0, n1 = KV tiles each tile visits (0 for a tile past T).
+// tiles, over the KV tiles [j0, j0 + cnt) of split sp (of S).  Q tile t visits
+// c_t of them (0 when its KV range ends before j0); cnt = 0 marks an empty
+// split, which every role skips.
 struct TcUnit {
-  int bh, b, hk, q0, n0, n1, nkv;
+  int bh, b, hk, q0, sp, j0, c0, c1, cnt;
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T) {
+__device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T, int S) {
   TcUnit u;
   const int BH = B * Hq;
   const int n_qb = (T + 255) >> 8;
-  const int qb = n_qb - 1 - idx / BH;  // last (longest when causal) row blocks first
-  u.bh = idx % BH;
+  u.sp = idx % S;
+  const int rest = idx / S;
+  const int qb = n_qb - 1 - rest / BH;  // last (longest when causal) row blocks first
+  u.bh = rest % BH;
   u.b = u.bh / Hq;
   const int h = u.bh - u.b * Hq;
   u.hk = h / (Hq / Hkv);
   u.q0 = qb * 256;
-  const int n_all = (T + 127) >> 7;
-  const int qs1 = u.q0 + 128;
-  u.n0 = CAUSAL ? min(n_all, (u.q0 >> 7) + 1) : n_all;
-  u.n1 = qs1 >= T ? 0 : (CAUSAL ? min(n_all, (qs1 >> 7) + 1) : n_all);
-  u.nkv = max(u.n0, u.n1);
+  int n0, n1;
+  tc_tile_counts(qb, T, CAUSAL, n0, n1);
+  const int nkv = max(n0, n1);
+  const int chunk = (nkv + S - 1) / S;  // KV tiles per split of this row block
+  u.j0 = u.sp * chunk;
+  const int j1 = min(nkv, u.j0 + chunk);
+  u.c0 = max(0, min(j1, n0) - u.j0);
+  u.c1 = max(0, min(j1, n1) - u.j0);
+  u.cnt = max(0, j1 - u.j0);
   return u;
 }
 
@@ -135,7 +153,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
                      float* __restrict__ LSE, int B, int Hq, int Hkv, int T, float scale_log2,
-                     int num_units) {
+                     int num_units, int S, float* __restrict__ part_o,
+                     float* __restrict__ part_lse) {
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
   constexpr int NSK = C::NSK, NSV = C::NSV;
@@ -244,9 +263,11 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
-          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T);
+          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T, S);
+          if (u.cnt == 0) continue;
           // Q of the previous unit is no longer read once its last S is done
-          if (k > 0 && !wait_bar(bar_qempty, (k - 1) & 1, abort_flag, &g_tc_err, kErrWaitLoad))
+          if (q_issued > 0 &&
+              !wait_bar(bar_qempty, (q_issued - 1) & 1, abort_flag, &g_tc_err, kErrWaitLoad))
             break;
           ptx::mbar_arrive_expect_tx(bar_qfull, 2 * TILE);
 #pragma unroll
@@ -255,9 +276,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             for (int bx = 0; bx < Tile::NBOX; ++bx)
               ptx::tma_load_3d_hint(sQ + t * TILE + bx * Tile::BOX_BYTES, &tmQ, bar_qfull, bx * 64,
                                     u.q0 + 128 * t, u.bh, pol_q);
-          q_issued = k + 1;
+          ++q_issued;
           const int zkv = u.b * Hkv + u.hk;
-          for (int j = 0; j < u.nkv; ++j) {
+          for (int j = u.j0; j < u.j0 + u.cnt; ++j) {
             const int sk = kc % NSK, sv = vc % NSV;
             if (kc >= NSK && !wait_bar(&bar_kempty[sk], ((kc / NSK) - 1) & 1, abort_flag,
                                        &g_tc_err, kErrWaitLoad)) {
@@ -301,12 +322,15 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         const uint32_t aV = ptx::smem_u32(sV);
         int kc = 0, vc = 0;              // K, V tiles consumed so far
         int pcnt0 = 0, pcnt1 = 0;        // P tiles consumed so far, per Q tile
+        int nu = 0;                      // units processed so far
         bool ok = true;
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
-          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T);
-          if (!wait_bar(bar_qfull, k & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
+          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T, S);
+          if (u.cnt == 0) continue;
+          if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
+          ++nu;
           ptx::tc_fence_after();
 
           // S_t = Q_t K_j^T; on an abort no further MMA is issued (the ones in
@@ -324,14 +348,14 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             ptx::mma_commit(&bar_sfull[t]);
             // the last S of KV tile j releases its K stage (tile 1 is last when
             // active); the unit's last S releases Q
-            if (t == 1 || j >= u.n1) ptx::mma_commit(&bar_kempty[st]);
-            if (j == u.nkv - 1 && (t == 1 || u.n1 < u.nkv)) ptx::mma_commit(bar_qempty);
+            if (t == 1 || j >= u.c1) ptx::mma_commit(&bar_kempty[st]);
+            if (j == u.cnt - 1 && (t == 1 || u.c1 < u.cnt)) ptx::mma_commit(bar_qempty);
             return true;
           };
 
-          if (ok && u.n0 > 0) ok = issue_s(0, 0);
-          if (ok && u.n1 > 0) ok = issue_s(1, 0);
-          for (int j = 0; ok && j < u.nkv; ++j) {
+          if (ok && u.c0 > 0) ok = issue_s(0, 0);
+          if (ok && u.c1 > 0) ok = issue_s(1, 0);
+          for (int j = 0; ok && j < u.cnt; ++j) {
             const int c = vc + j;
             const int sv = c % NSV;
             if (!wait_bar(&bar_vfull[sv], (c / NSV) & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
@@ -341,7 +365,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              const int nt = t == 0 ? u.n0 : u.n1;
+              const int nt = t == 0 ? u.c0 : u.c1;
               if (ok && j < nt) {
                 int& pc = t == 0 ? pcnt0 : pcnt1;
                 if (!wait_bar(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
@@ -356,14 +380,14 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                               Tile::mnmajor_desc(aV + sv * TILE, kk), IDESC_PV,
                               (j > 0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(&bar_odone[t]);
-                const bool last_pv = (t == 1) || !(j < u.n1);
+                const bool last_pv = (t == 1) || !(j < u.c1);
                 if (last_pv) ptx::mma_commit(&bar_vempty[sv]);
                 if (j + 1 < nt) ok = issue_s(t, j + 1);
               }
             }
           }
-          kc += u.nkv;
-          vc += u.nkv;
+          kc += u.cnt;
+          vc += u.cnt;
         }
         ptx::mma_commit(bar_final);
         drain_bar(bar_final, 0, &g_tc_err);
@@ -392,8 +416,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     for (int k = 0; ok; ++k) {
       const int idx = tc_unit_index(k);
       if (idx >= num_units) break;
-      const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T);
-      const int n = t == 0 ? u.n0 : u.n1;
+      const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T, S);
+      const int n = t == 0 ? u.c0 : u.c1;
       const int q_start = u.q0 + 128 * t;
       const int grow = q_start + row;
       float m_ref = -INFINITY;
@@ -416,7 +440,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         // masked scores become -inf (+inf when scale < 0), so that their
         // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
         // never 0: the host passes the smallest normal float for scale = 0)
-        const int kb = j * 128;
+        const int kb = (u.j0 + j) * 128;
         const bool masked = (kb + 127 >= T) || (CAUSAL && kb + 127 > q_start);
         if (masked) {
           const int lim = CAUSAL ? min(T - 1, grow) - kb : T - 1 - kb;  // last kept column
@@ -519,6 +543,39 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = grow < T;
+      if (part_o != nullptr) {
+        // split of the KV range: normalised fp32 partial O and its LSE; the
+        // combine kernel merges the splits
+        const size_t prow = static_cast<size_t>(u.sp) * B * Hq * T +
+                            static_cast<size_t>(u.bh) * T + (row_ok ? grow : 0);
+        float* po = part_o + prow * D;
+#pragma unroll
+        for (int oc = 0; oc < (D + 31) / 32; ++oc) {
+          uint32_t o[32];
+          if constexpr (D >= 32) {
+            ptx::tmem_ld32(tO + oc * 32, o);
+            ptx::tmem_ld_wait(o);
+          } else {
+            uint32_t h16[16];
+            ptx::tmem_ld16(tO, h16);
+            ptx::tmem_ld_wait(h16);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) o[v] = h16[v];
+          }
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(po + oc * 32);
+#pragma unroll
+            for (int w = 0; w < (D >= 32 ? 8 : 4); ++w)
+              dst[w] = make_float4(__uint_as_float(o[4 * w]) * inv_l,
+                                   __uint_as_float(o[4 * w + 1]) * inv_l,
+                                   __uint_as_float(o[4 * w + 2]) * inv_l,
+                                   __uint_as_float(o[4 * w + 3]) * inv_l);
+          }
+        }
+        if (row_ok) part_lse[prow] = (m_ref + log2f(l)) * 0.6931471805599453f;
+        ptx::tc_fence_before();
+        continue;
+      }
       uint16_t* orow = O + (static_cast<size_t>(u.bh) * T + (row_ok ? grow : 0)) * D;
       if constexpr (D >= 32) {
 #pragma unroll
@@ -576,8 +633,62 @@ static int tc_sm_count() {
   return cache[dev];
 }
 
+// Merge of the KV splits of one query row (one warp per row): with the
+// splits' normalised partial outputs O_s and log-sum-exps L_s,
+//   L = m + ln sum_s exp(L_s - m),  m = max_s L_s,
+//   O = sum_s exp(L_s - L) O_s,
+// the same online-softmax rescaling, applied across splits instead of tiles.
+// Only the splits whose KV range reaches the row's tile are read.
+template <bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(256)
+    fa_split_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                            uint16_t* __restrict__ O, float* __restrict__ LSE, int BH, int T,
+                            int D, int S) {
+  const long long rows = static_cast<long long>(BH) * T;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int r = static_cast<int>(row % T);
+  int n0, n1;
+  tc_tile_counts(r >> 8, T, CAUSAL, n0, n1);
+  const int nkv = max(n0, n1);
+  const int nt = ((r >> 7) & 1) ? n1 : n0;
+  const int chunk = (nkv + S - 1) / S;
+  const int ns = min(S, (nt + chunk - 1) / chunk);  // splits that hold this row
+  float m = -INFINITY;
+  for (int sp = 0; sp < ns; ++sp) m = fmaxf(m, part_lse[sp * rows + row]);
+  float wsum = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int sp = 0; sp < ns; ++sp) {
+    const float w = expf(part_lse[sp * rows + row] - m);
+    wsum += w;
+    const float* po = part_o + (sp * rows + row) * D;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = lane + 32 * i;
+      if (c < D) acc[i] = fmaf(w, po[c], acc[i]);
+    }
+  }
+  const float inv = 1.f / wsum;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;
+    if (c < D) {
+      const float y = acc[i] * inv;
+      if constexpr (F16) {
+        const __half hv = __float2half_rn(y);
+        O[row * D + c] = *reinterpret_cast<const uint16_t*>(&hv);
+      } else {
+        const __nv_bfloat16 hv = __float2bfloat16_rn(y);
+        O[row * D + c] = *reinterpret_cast<const uint16_t*>(&hv);
+      }
+    }
+  }
+  if (lane == 0) LSE[row] = m + logf(wsum);
+}
+
 template <int D, bool CAUSAL, bool F16>
-static fa_status launch_tc_impl(const FwdArgs& a) {
+static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* part_lse) {
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
   auto kern = fa_fwd_tc_kernel<D, CAUSAL, F16>;
@@ -605,7 +716,7 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
   if ((r = make_tmap_16bit(&mv, a.v, D, a.T, static_cast<long long>(a.B) * a.Hkv, Tile::BOX_X,
                            Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
     return cu_status(r);
-  const long long units = static_cast<long long>(a.B) * a.Hq * ((a.T + 255) / 256);
+  const long long units = static_cast<long long>(a.B) * a.Hq * ((a.T + 255) / 256) * S;
   const long long grid = units < tc_sm_count() ? units : tc_sm_count();  // one CTA per SM
   // scale * log2(e); never exactly 0, so that masked (infinite) scores give
   // exponents of -inf rather than NaN: for scale = 0 the smallest normal
@@ -614,26 +725,68 @@ static fa_status launch_tc_impl(const FwdArgs& a) {
   if (scale_log2 == 0.f) scale_log2 = 1.17549435e-38f;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, static_cast<uint16_t*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
-      static_cast<int>(units));
+      static_cast<int>(units), S, S > 1 ? part_o : nullptr, S > 1 ? part_lse : nullptr);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || S == 1) return cuda_status(e);
+  const long long rows = static_cast<long long>(a.B) * a.Hq * a.T;
+  fa_split_combine_kernel<CAUSAL, F16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0,
+                                         a.stream>>>(part_o, part_lse,
+                                                     static_cast<uint16_t*>(a.o), a.lse,
+                                                     a.B * a.Hq, a.T, D, S);
   return cuda_status(cudaGetLastError());
 }
 
 template <bool F16>
-static fa_status launch_tc_t(const FwdArgs& a) {
+static fa_status launch_tc_t(const FwdArgs& a, int S, float* po, float* pl) {
   const bool c = a.causal != 0;
   switch (a.d) {
-    case 16: return c ? launch_tc_impl<16, true, F16>(a) : launch_tc_impl<16, false, F16>(a);
-    case 32: return c ? launch_tc_impl<32, true, F16>(a) : launch_tc_impl<32, false, F16>(a);
-    case 64: return c ? launch_tc_impl<64, true, F16>(a) : launch_tc_impl<64, false, F16>(a);
-    case 128: return c ? launch_tc_impl<128, true, F16>(a) : launch_tc_impl<128, false, F16>(a);
+    case 16:
+      return c ? launch_tc_impl<16, true, F16>(a, S, po, pl) : launch_tc_impl<16, false, F16>(a, S, po, pl);
+    case 32:
+      return c ? launch_tc_impl<32, true, F16>(a, S, po, pl) : launch_tc_impl<32, false, F16>(a, S, po, pl);
+    case 64:
+      return c ? launch_tc_impl<64, true, F16>(a, S, po, pl) : launch_tc_impl<64, false, F16>(a, S, po, pl);
+    case 128:
+      return c ? launch_tc_impl<128, true, F16>(a, S, po, pl)
+               : launch_tc_impl<128, false, F16>(a, S, po, pl);
     default: return FA_ERR_UNSUPPORTED;
   }
 }
 
-fa_status launch_tc(const FwdArgs& a) {
-  if (a.dtype == FA_DTYPE_BF16) return launch_tc_t<false>(a);
-  if (a.dtype == FA_DTYPE_F16) return launch_tc_t<true>(a);
+fa_status launch_tc(const FwdArgs& a) { return launch_tc_split(a, 1, nullptr, 0); }
+
+fa_status launch_tc_split(const FwdArgs& a, int S, void* workspace, size_t workspace_bytes) {
+  float* po = nullptr;
+  float* pl = nullptr;
+  if (S > 1) {
+    const size_t need = split_workspace_bytes(a.B, a.Hq, a.T, a.d, S);
+    if (workspace == nullptr || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    po = static_cast<float*>(workspace);
+    pl = po + static_cast<size_t>(S) * a.B * a.Hq * a.T * a.d;
+  }
+  if (a.dtype == FA_DTYPE_BF16) return launch_tc_t<false>(a, S, po, pl);
+  if (a.dtype == FA_DTYPE_F16) return launch_tc_t<true>(a, S, po, pl);
   return FA_ERR_UNSUPPORTED;
+}
+
+size_t split_workspace_bytes(int B, int Hq, int T, int d, int S) {
+  // partial O (fp32) then partial LSE (fp32) of every split
+  return static_cast<size_t>(S) * B * Hq * T * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+int split_heuristic(int B, int Hq, int T, int causal) {
+  // split the KV range only when the row blocks leave more than half of the
+  // SMs idle; then aim at about one unit per SM, with at least 4 KV tiles per
+  // split (shorter ones are launch-latency bound and lose to the extra merge)
+  const long long units = static_cast<long long>(B) * Hq * ((T + 255) / 256);
+  const int sm = tc_sm_count();
+  if (units * 2 > sm) return 1;
+  const int n_all = (T + 127) / 128;
+  long long s = (sm + units - 1) / units;
+  if (s > n_all / 4) s = n_all / 4;
+  if (s > kMaxSplits) s = kMaxSplits;
+  (void)causal;
+  return s < 2 ? 1 : static_cast<int>(s);
 }
 
 fa_status tc_read_and_clear_error(unsigned int* word) {

@@ -57,8 +57,9 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2, /* d not in {16,32,64,128} or unknown dtype */
   FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch etc.) */
-  FA_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a barrier (reported
+  FA_ERR_TIMEOUT = 5,     /* a kernel gave up waiting on a barrier (reported
                              by fa_debug_sync_check only) */
+  FA_ERR_WORKSPACE = 6    /* the scratch workspace is missing or too small */
 } fa_status;
 
 typedef enum { FA_DTYPE_F32 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_F16 = 2 } fa_dtype;
@@ -75,6 +76,39 @@ typedef enum { FA_DTYPE_F32 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_F16 = 2 } fa_dtype;
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int Hq, int Hkv, int T, int d, float scale, int causal,
                  fa_dtype dtype, void* stream);
+
+/* Split-KV forward (FlashDecoding-style; "Flash Attention Memory Optimization
+ * Explained", section "Why It Matters", names FlashDecoding as the inference
+ * extension).  Same operation, arguments and results as fa_fwd, for shapes
+ * with too few (batch, head, 256-row block) work units to fill the GPU: the
+ * keys of every row block are cut into num_splits contiguous ranges that run
+ * on different SMs; each writes its normalised partial output O_s and
+ * log-sum-exp L_s to `workspace`, and a second kernel merges them exactly,
+ * L = m + ln sum_s exp(L_s - m) (m = max_s L_s), O = sum_s exp(L_s - L) O_s.
+ *   num_splits : 1 .. 64 (1 = fa_fwd; fa_fwd_split_heuristic suggests one)
+ *   workspace  : DEVICE scratch of at least fa_fwd_split_workspace_size(...)
+ *                bytes, 16-byte aligned, not overlapping any other buffer;
+ *                owned by the caller, contents on entry are ignored and on
+ *                return are undefined; unused when num_splits = 1
+ * fp32 inputs run the CUDA-core kernel, which needs no split (workspace
+ * unused).  Errors: as fa_fwd, plus FA_ERR_INVALID_ARG for num_splits outside
+ * 1..64 or an overlapping workspace, FA_ERR_WORKSPACE when num_splits > 1 and
+ * the workspace is NULL or too small.  Calls that share a workspace and run
+ * concurrently on the GPU race. */
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                       fa_dtype dtype, int num_splits, void* workspace,
+                       unsigned long long workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_fwd_split needs (num_splits * B * Hq * T * (d + 1) *
+ * 4: fp32 partial outputs and log-sum-exps); 0 for invalid sizes. */
+unsigned long long fa_fwd_split_workspace_size(int B, int Hq, int T, int d, int num_splits);
+
+/* A split count for this shape on the current device: 1 when the row blocks
+ * already occupy at least half of the SMs, else about one work unit per SM
+ * with at least four 128-key tiles per split (at most 64 splits).  Returns 1
+ * on invalid sizes. */
+int fa_fwd_split_heuristic(int B, int Hq, int Hkv, int T, int d, int causal);
 
 /* Static English text for a status code (never NULL). */
 const char* fa_status_string(fa_status s);

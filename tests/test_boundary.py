@@ -37,7 +37,8 @@ def test_headers_declare_the_abi():
     names = declared_functions()
     for n in ("fa_fwd", "fa_status_string", "fa_version", "fa_debug_sync_check",
               "fa_last_cuda_error", "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout",
-              "fa_fwd_simt"):
+              "fa_fwd_simt", "fa_fwd_split", "fa_fwd_split_workspace_size",
+              "fa_fwd_split_heuristic"):
         assert n in names
 
 
@@ -53,7 +54,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert fa.fa_version() == 10000
-    for s in range(6):
+    for s in range(7):
         txt = fa.fa_status_string(s)
         assert isinstance(txt, str) and txt
     assert fa.fa_status_string(0) == "ok"
@@ -138,3 +139,42 @@ def test_exported_symbols_have_c_linkage(lib):
     # a C++-mangled name would not be found by its plain name
     for n in declared_functions():
         assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+WS = BASE + (6 << 36)
+
+
+def split_call(num_splits=4, ws=WS, ws_bytes=None, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = fa.fa_fwd_split_workspace_size(a["B"], a["Hq"], a["T"], a["d"], num_splits)
+    return fa.fa_fwd_split(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                           a["T"], a["d"], a["scale"], a["causal"], a["dtype"], num_splits, ws,
+                           ws_bytes, stream=0)
+
+
+def test_split_workspace_size_and_heuristic(lib):
+    # num_splits * B * Hq * T * (d + 1) * 4 bytes
+    assert fa.fa_fwd_split_workspace_size(2, 4, 100, 64, 3) == 3 * 2 * 4 * 100 * 65 * 4
+    assert fa.fa_fwd_split_workspace_size(2, 4, 100, 64, 0) == 0
+    assert fa.fa_fwd_split_workspace_size(2, 4, 100, 64, 65) == 0
+    assert fa.fa_fwd_split_workspace_size(0, 4, 100, 64, 2) == 0
+    # many row blocks: no split; a single small head: split, at most one per KV tile
+    assert fa.fa_fwd_split_heuristic(64, 1, 1, 4096, 128, 1) == 1
+    s = fa.fa_fwd_split_heuristic(1, 1, 1, 4096, 128, 1)
+    assert 2 <= s <= 8                                          # >= 4 of the 32 KV tiles each
+    assert fa.fa_fwd_split_heuristic(1, 1, 1, 1024, 64, 0) == 2
+    assert fa.fa_fwd_split_heuristic(1, 1, 1, 200, 64, 0) == 1  # too short to split
+    assert fa.fa_fwd_split_heuristic(0, 1, 1, 200, 64, 0) == 1
+
+
+def test_split_rejects_bad_arguments_on_the_host(lib):
+    assert split_call(num_splits=0) == fa.FA_ERR_INVALID_ARG
+    assert split_call(num_splits=65) == fa.FA_ERR_INVALID_ARG
+    assert split_call(ws=0) == fa.FA_ERR_WORKSPACE
+    assert split_call(ws_bytes=1000) == fa.FA_ERR_WORKSPACE
+    assert split_call(ws=WS + 8) == fa.FA_ERR_MISALIGNED
+    assert split_call(ws=O) == fa.FA_ERR_INVALID_ARG        # workspace overlaps O
+    assert split_call(q=0) == fa.FA_ERR_INVALID_ARG         # the fa_fwd checks apply too
+    assert split_call(d=48) == fa.FA_ERR_UNSUPPORTED

@@ -104,6 +104,37 @@ def test_full_parity_growing_row_max(cuda_lib, d, dtype):
         assert np.all(el <= bound), f"ramp d={d} {dtype}: max|dL|={el.max():.3g}"
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T,d,splits", [(1000, 128, 2), (1000, 64, 3), (777, 32, 5),
+                                        (4096, 128, 8), (300, 16, 4), (129, 128, 2),
+                                        (2048, 64, 64)])
+def test_split_kv_parity(cuda_lib, T, d, splits, causal, dtype):
+    """Split-KV forward (partials merged by log-sum-exp weights) against the
+    oracle, including more splits than KV tiles (empty splits) and ragged T."""
+    fa = cuda_lib
+    q, k, v = make_qkv(1, 4, 2, T, d, dtype=dtype, seed=T + d + splits, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+    check_full(o, lse, q, k, v, scale, causal, what=f"split={splits} T={T} d={d} {dtype}")
+
+
+def test_split_heuristic_path_matches_unsplit(cuda_lib):
+    """A shape the heuristic splits (one head of T = 4096) gives the oracle's
+    result and agrees with the unsplit kernel."""
+    fa = cuda_lib
+    q, k, v = make_qkv(1, 1, 1, 4096, 128, dtype="bf16", seed=21, device="cuda")
+    assert fa.fa_fwd_split_heuristic(1, 1, 1, 4096, 128, 1) > 1
+    o1, l1 = run(fa, q, k, v, True)
+    o2, l2 = fa.fwd(q, k, v, causal=True, num_splits=1)
+    torch.cuda.synchronize()
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    assert (l1 - l2).abs().max().item() <= 2e-3
+    check_full(o1, l1, q, k, v, 1 / math.sqrt(128), True, what="heuristic split")
+
+
 def test_causal_row0_and_zero_query_closed_forms(cuda_lib):
     """Closed forms on the device: causal row 0 returns V[0] (exactly, up to
     output rounding) and Q = 0 gives LSE[i] = ln(i+1)."""
