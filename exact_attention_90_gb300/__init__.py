@@ -26,6 +26,7 @@ __all__ = [
     "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
     "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_split",
+    "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
@@ -58,6 +59,7 @@ EXPORTS = [
     ("fa_unit_timeout", _I, [ctypes.c_longlong, _P, _P]),
     ("fa_fwd_split", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
                           ctypes.c_ulonglong, _P]),
+    ("fa_fwd_split_static", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     ("fa_fwd_split_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I]),
     ("fa_fwd_split_heuristic", _I, [_I, _I, _I, _I, _I, _I]),
     ("fa_fwd_simt", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
@@ -147,6 +149,18 @@ def fa_fwd_split(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, num_sp
                             int(Hkv), int(T), int(d), float(scale), int(causal), int(dtype),
                             int(num_splits), _ptr(workspace), int(workspace_bytes),
                             _stream(stream))
+
+
+def fa_fwd_split_static(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, num_splits,
+                        stream=None) -> int:
+    """The C function fa_fwd_split_static: split-KV forward for callers that
+    cannot allocate device memory (a host application's own memory pool, or a
+    path that cannot afford cudaMalloc's synchronisation); its scratch is a
+    fixed 64 MiB array inside the library."""
+    lib = load_library()
+    return lib.fa_fwd_split_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                   int(Hq), int(Hkv), int(T), int(d), float(scale), int(causal),
+                                   int(dtype), int(num_splits), _stream(stream))
 
 
 def fa_fwd_split_workspace_size(B, Hq, T, d, num_splits) -> int:

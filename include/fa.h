@@ -100,6 +100,27 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
                        fa_dtype dtype, int num_splits, void* workspace,
                        unsigned long long workspace_bytes, void* stream);
 
+/* fa_fwd_split for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is an interface choice of this library.)  Some
+ * callers cannot call cudaMalloc: a plugin hosted by an application that
+ * hands out all device memory through its own pool, where a raw cudaMalloc
+ * would bypass the pool's accounting or fail once the pool has reserved the
+ * device, or a latency-critical path that cannot afford cudaMalloc's implicit
+ * device-wide synchronisation.  This entry point takes no workspace: its
+ * scratch is a fixed 64 MiB array inside the library (every GPU that loads
+ * libfa.so holds it until the process exits).  Arguments, results and errors
+ * are those of fa_fwd_split without the workspace, plus FA_ERR_WORKSPACE when
+ * fa_fwd_split_workspace_size(B, Hq, T, d, num_splits) exceeds 64 MiB (use a
+ * smaller num_splits, or 1, which needs no scratch).
+ * Set-up: the first call on each device looks up the scratch array's device
+ * address (cudaGetSymbolAddress, no allocation); make that first call before
+ * any stream capture.  Every call on a device shares the one array and leaves
+ * its partial results there; no call relies on earlier contents, but calls
+ * that overlap on the GPU (for example on different streams) race. */
+fa_status fa_fwd_split_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                              fa_dtype dtype, int num_splits, void* stream);
+
 /* Bytes of workspace fa_fwd_split needs (num_splits * B * Hq * T * (d + 1) *
  * 4: fp32 partial outputs and log-sum-exps); 0 for invalid sizes. */
 unsigned long long fa_fwd_split_workspace_size(int B, int Hq, int T, int d, int num_splits);
