@@ -341,10 +341,13 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             if (!wait_bar(&bar_kfull[st], (c / NSK) & 1, abort_flag, &g_tc_err, kErrWaitMma))
               return false;
             ptx::tc_fence_after();
+            const uint32_t qlo = Tile::kmajor_lo(aQ + t * TILE);
+            const uint32_t klo = Tile::kmajor_lo(aK + st * TILE);
 #pragma unroll
             for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
-              ptx::mma_ss(tmem + C::COL_S0 + t * 128, Tile::kmajor_desc(aQ + t * TILE, kk),
-                          Tile::kmajor_desc(aK + st * TILE, kk), IDESC_QK, kk > 0 ? 1u : 0u);
+              ptx::mma_ss_lh(tmem + C::COL_S0 + t * 128, qlo + Tile::kmajor_step(kk),
+                             Tile::DESC_HI, klo + Tile::kmajor_step(kk), Tile::DESC_HI, IDESC_QK,
+                             kk > 0 ? 1u : 0u);
             ptx::mma_commit(&bar_sfull[t]);
             // the last S of KV tile j releases its K stage (tile 1 is last when
             // active); the unit's last S releases Q
@@ -374,11 +377,12 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                 }
                 ++pc;
                 ptx::tc_fence_after();
+                const uint32_t vlo = Tile::mnmajor_lo(aV + sv * TILE);
 #pragma unroll
                 for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
-                  ptx::mma_ts(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
-                              Tile::mnmajor_desc(aV + sv * TILE, kk), IDESC_PV,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+                  ptx::mma_ts_lh(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
+                                 vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(&bar_odone[t]);
                 const bool last_pv = (t == 1) || !(j < u.c1);
                 if (last_pv) ptx::mma_commit(&bar_vempty[sv]);

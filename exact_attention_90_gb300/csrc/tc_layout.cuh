@@ -40,6 +40,25 @@ struct TcTile {
   // matching CUtensorMapSwizzle value: 1 = 32B, 2 = 64B, 3 = 128B
   static constexpr int TMA_SWIZZLE = ROW_BYTES == 128 ? 3 : (ROW_BYTES == 64 ? 2 : 1);
 
+  // Descriptor halves.  A shared-memory address is below 2^18, so its 14-bit
+  // start-address field never carries into the LBO field: the low word of a
+  // k-step's descriptor is the tile's low word plus (byte offset >> 4).
+  static constexpr uint32_t DESC_HI = (SBO >> 4) | (1u << 14) | (LAYOUT << 29);
+  static constexpr uint32_t KM_LO_LBO = (16u >> 4) << 16;
+  static constexpr uint32_t MN_LO_LBO = (static_cast<uint32_t>(BOX_BYTES) >> 4) << 16;
+  __device__ static __forceinline__ uint32_t kmajor_lo(uint32_t base) {
+    return (base >> 4) | KM_LO_LBO;
+  }
+  __device__ static __forceinline__ uint32_t mnmajor_lo(uint32_t base) {
+    return (base >> 4) | MN_LO_LBO;
+  }
+  static constexpr uint32_t kmajor_step(int kk) {
+    return static_cast<uint32_t>((kk / KSTEPS_PER_BOX) * BOX_BYTES + (kk % KSTEPS_PER_BOX) * 32) >> 4;
+  }
+  static constexpr uint32_t mnmajor_step(int kk) {
+    return static_cast<uint32_t>(kk * 16 * ROW_BYTES) >> 4;
+  }
+
   // K-major operand (Q or K tile at shared address `base`), k-step kk.
   __device__ static __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
     const uint32_t addr =
