@@ -433,13 +433,10 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                         wait_bar(&bar_sfull[t], it & 1, abort_flag, &g_tc_err, kErrWaitSoftmax));
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s[c]);
-        ptx::tmem_ld_wait(s[0]);
-        ptx::reg_fence(s[1]);
-        ptx::reg_fence(s[2]);
-        ptx::reg_fence(s[3]);
+        uint32_t sflat[128];
+        ptx::tmem_ld128(tS, sflat);
+        ptx::tmem_ld_wait(sflat);
+        uint32_t(&s)[4][32] = *reinterpret_cast<uint32_t(*)[4][32]>(&sflat);
 
         // masked scores become -inf (+inf when scale < 0), so that their
         // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
@@ -487,9 +484,10 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         const uint64_t sl2x2 = ptx::f2_pack(scale_log2, scale_log2);
         const uint64_t nmox2 = ptx::f2_pack(-mo, -mo);
         uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+        uint32_t pall[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+          uint32_t(&pk)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pall[16 * c]);
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
             const uint64_t x2 = ptx::fma2(
@@ -501,8 +499,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             acc2[v & 1] = ptx::add2(acc2[v & 1], ptx::f2_pack(p0, p1));
             pk[v] = ptx::pack_x2<F16>(p0, p1);
           }
-          ptx::tmem_st16(tS + c * 16, pk);
         }
+        ptx::tmem_st64(tS, pall);
         // O correction (lazy, warp-uniform), before P is released: the next
         // P.V MMA accumulates into O
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
