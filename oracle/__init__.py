@@ -37,6 +37,7 @@ from .attention_ref import (
     attention_rows_ref,
     kv_head_of,
     naive_score_bytes,
+    valid_keys,
 )
 from .brute import attention_brute
 from .online_ref import attention_online_ref
@@ -50,4 +51,5 @@ __all__ = [
     "attention_brute",
     "kv_head_of",
     "naive_score_bytes",
+    "valid_keys",
 ]

@@ -43,6 +43,11 @@ Readings of points the pages leave open or print inconsistently:
   * scale multiplies the fp64 score; the naive listing divides scores by
     sqrt(d) and the kernel multiplies Q by the scale before the dot: both are
     the same real number, the oracle takes the plain definition.
+  * sliding windows: [tri] "1. 稀疏注意力支持" keeps key j for query i when
+    |i - j| <= window_size.  The oracle takes a band window = (wl, wr): keep j
+    when i - wl <= j <= i + wr, -1 meaning unbounded on that side; the page's
+    window is (w, w), causal attention is (-1, 0), and `causal` combines with
+    a window by intersection.
   * MQA/GQA: [tri] "2. 多查詢注意力（MQA）" broadcasts a single KV head to all
     query heads; the grouped generalisation maps query head h to KV head
     h // (Hq // Hkv) (equivalently repeat_interleave of K, V along heads).
@@ -87,7 +92,23 @@ def _check_shapes(q, k, v):
     return B, Hq, Hkv, T, d
 
 
-def _rows_of_head(qh, kh, vh, rows, scale, causal):
+def valid_keys(rows, T, causal, window=None):
+    """Boolean [len(rows), T]: key j is kept for query row i (the mask)."""
+    j = np.arange(T)[None, :]
+    i = np.asarray(rows)[:, None]
+    valid = np.ones((len(rows), T), dtype=bool)
+    if causal:
+        valid &= j <= i                               # keep j <= i
+    if window is not None:
+        wl, wr = window
+        if wl >= 0:
+            valid &= j >= i - wl
+        if wr >= 0:
+            valid &= j <= i + wr
+    return valid
+
+
+def _rows_of_head(qh, kh, vh, rows, scale, causal, window=None):
     """The four naive steps for the query rows ``rows`` of one head (fp64).
 
     Step 1 (scores) and step 4 (weighted sum) are dense products; steps 2 and 3
@@ -97,10 +118,7 @@ def _rows_of_head(qh, kh, vh, rows, scale, causal):
     """
     T = kh.shape[0]
     s = (qh[rows] @ kh.T) * scale                     # step 1 + scale
-    if causal:
-        valid = np.arange(T)[None, :] <= rows[:, None]  # keep j <= i
-    else:
-        valid = np.ones((len(rows), T), dtype=bool)
+    valid = valid_keys(rows, T, causal, window)
     s = np.where(valid, s, -np.inf)                   # step 2: mask (excluded)
     m = s.max(axis=1)                                 # row maximum
     e = np.where(valid, np.exp(s - m[:, None]), 0.0)  # step 3: softmax numerator
@@ -110,7 +128,7 @@ def _rows_of_head(qh, kh, vh, rows, scale, causal):
     return o, lse, e / l[:, None]
 
 
-def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256):
+def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256, window=None):
     """Exact attention forward by its definition, fp64.
 
     Args:
@@ -119,6 +137,9 @@ def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256):
       causal: keep key j for query i iff j <= i.
       row_chunk: rows of S formed at once (memory O(row_chunk * T)); only the
         grouping of independent rows, no reordering of any sum.
+      window: optional band (wl, wr): keep key j for query i iff
+        i - wl <= j <= i + wr (-1 = unbounded side); every row must keep at
+        least one key (true whenever wl, wr are -1 or >= 0).
 
     Returns:
       (O, LSE): O [B, Hq, T, d] fp64, LSE [B, Hq, T] fp64 (natural log).
@@ -132,13 +153,14 @@ def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256):
             hk = kv_head_of(h, Hq, Hkv)
             for r0 in range(0, T, row_chunk):
                 rows = np.arange(r0, min(T, r0 + row_chunk))
-                o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal)
+                o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal,
+                                          window)
                 O[b, h, rows] = o
                 L[b, h, rows] = lse
     return O, L
 
 
-def attention_rows_ref(q, k, v, scale: float, causal: bool, b: int, h: int, rows):
+def attention_rows_ref(q, k, v, scale: float, causal: bool, b: int, h: int, rows, window=None):
     """The definition evaluated for selected query rows of one (b, h) only.
 
     Used for parity at full workload sizes, where the whole oracle would take
@@ -153,11 +175,11 @@ def attention_rows_ref(q, k, v, scale: float, causal: bool, b: int, h: int, rows
     if rows.size and (rows.min() < 0 or rows.max() >= T):
         raise ValueError("row index out of range")
     hk = kv_head_of(h, Hq, Hkv)
-    o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal)
+    o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal, window)
     return o, lse
 
 
-def attention_probs_ref(q, k, v, scale: float, causal: bool):
+def attention_probs_ref(q, k, v, scale: float, causal: bool, window=None):
     """The full probability matrix P [B, Hq, T, T] (fp64); small cases only."""
     q, k, v = as_f64(q), as_f64(k), as_f64(v)
     B, Hq, Hkv, T, d = _check_shapes(q, k, v)
@@ -166,7 +188,7 @@ def attention_probs_ref(q, k, v, scale: float, causal: bool):
     for b in range(B):
         for h in range(Hq):
             hk = kv_head_of(h, Hq, Hkv)
-            _, _, p = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal)
+            _, _, p = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal, window)
             P[b, h] = p
     return P
 

@@ -30,8 +30,12 @@ def _to_nested(x):
     return x
 
 
-def attention_brute(q, k, v, scale: float, causal: bool):
-    """Returns (O, LSE) as nested Python lists [B][Hq][T][d] and [B][Hq][T]."""
+def attention_brute(q, k, v, scale: float, causal: bool, window=None):
+    """Returns (O, LSE) as nested Python lists [B][Hq][T][d] and [B][Hq][T].
+
+    window = (wl, wr) keeps, in addition, only keys i - wl <= j <= i + wr
+    (-1 = unbounded side), the band form of the tutorial's sliding window.
+    """
     q, k, v = _to_nested(q), _to_nested(k), _to_nested(v)
     B, Hq, T, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     Hkv = len(k[0])
@@ -44,7 +48,16 @@ def attention_brute(q, k, v, scale: float, causal: bool):
         for h in range(Hq):
             hk = h // group
             for i in range(T):
-                keys = [j for j in range(T) if (not causal or j <= i)]
+                keys = []
+                for j in range(T):
+                    if causal and j > i:
+                        continue
+                    if window is not None:
+                        if window[0] >= 0 and j < i - window[0]:
+                            continue
+                        if window[1] >= 0 and j > i + window[1]:
+                            continue
+                    keys.append(j)
                 scores = {}
                 for j in keys:
                     dot = math.fsum(q[b][h][i][c] * k[b][hk][j][c] for c in range(d))

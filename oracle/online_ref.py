@@ -30,7 +30,7 @@ import numpy as np
 from .attention_ref import as_f64, kv_head_of
 
 
-def attention_online_ref(q, k, v, scale: float, causal: bool, block_sizes):
+def attention_online_ref(q, k, v, scale: float, causal: bool, block_sizes, window=None):
     """O and LSE by the block recurrence.
 
     Args:
@@ -59,8 +59,15 @@ def attention_online_ref(q, k, v, scale: float, causal: bool, block_sizes):
                 c1 = min(T, c0 + sizes[n % len(sizes)])
                 cols = np.arange(c0, c1)
                 s = (qh @ kh[c0:c1].T) * scale
+                keep = np.ones(s.shape, dtype=bool)
                 if causal:
-                    s = np.where(rows[:, None] >= cols[None, :], s, -np.inf)
+                    keep &= rows[:, None] >= cols[None, :]
+                if window is not None:
+                    if window[0] >= 0:
+                        keep &= cols[None, :] >= rows[:, None] - window[0]
+                    if window[1] >= 0:
+                        keep &= cols[None, :] <= rows[:, None] + window[1]
+                s = np.where(keep, s, -np.inf)
                 m_new = np.maximum(m, s.max(axis=1))
                 # a row that has seen only masked keys keeps m = -inf; its
                 # correction factor and probabilities are then 0 by definition

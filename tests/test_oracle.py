@@ -169,9 +169,60 @@ def pin_head_mapping_brute(ref):
         np.testing.assert_allclose(L, np.array(Lb), rtol=0, atol=1e-13)
 
 
+def pin_window_library_sdpa(ref):
+    """Band windows against torch's scaled_dot_product_attention (CPU,
+    float64) with the explicit boolean mask |i - j| <= w of the tutorial's
+    sliding_window_mask, and asymmetric bands, causal or not."""
+    for (T, d, window, causal) in ((40, 8, (3, 3), False), (40, 8, (5, 0), False),
+                                   (33, 16, (7, 2), True), (64, 8, (0, 10), False),
+                                   (50, 4, (-1, 4), False), (50, 4, (6, -1), True)):
+        q, k, v = _rand(1, 2, 2, T, d, seed=T + d + window[0])
+        O, L = ref(q, k, v, 0.4, causal, window=window)
+        i = torch.arange(T)[:, None]
+        j = torch.arange(T)[None, :]
+        keep = torch.ones(T, T, dtype=torch.bool)
+        if causal:
+            keep &= j <= i
+        if window[0] >= 0:
+            keep &= j >= i - window[0]
+        if window[1] >= 0:
+            keep &= j <= i + window[1]
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        Ot = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=keep, scale=0.4)
+        np.testing.assert_allclose(O, Ot.numpy(), rtol=0, atol=1e-12)
+        sc = (torch.einsum("bhid,bhjd->bhij", tq, tk) * 0.4).masked_fill(~keep, float("-inf"))
+        np.testing.assert_allclose(L, torch.logsumexp(sc, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_window_closed_forms(ref):
+    """Window (0, 0): each row attends only to itself, so O[i] = V[i] and
+    LSE[i] = scale * q_i . k_i; a window wider than T is no window."""
+    q, k, v = _rand(1, 2, 2, 17, 8, seed=71)
+    O, L = ref(q, k, v, 0.3, False, window=(0, 0))
+    np.testing.assert_array_equal(O, v)
+    np.testing.assert_allclose(L, 0.3 * np.einsum("bhid,bhid->bhi", q, k), rtol=0, atol=1e-13)
+    O1, L1 = ref(q, k, v, 0.3, True, window=(100, 100))
+    O2, L2 = ref(q, k, v, 0.3, True)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
+
+
+def pin_window_brute(ref):
+    """Windows against the scalar restatement on tiny shapes."""
+    for T in (3, 6, 8):
+        for window in ((0, 1), (2, 2), (1, -1), (-1, 1)):
+            for causal in (False, True):
+                q, k, v = _rand(1, 2, 1, T, 3, seed=T * 11 + window[0] + 2 * window[1])
+                O, L = ref(q, k, v, 0.8, causal, window=window)
+                Ob, Lb = oracle.attention_brute(q, k, v, 0.8, causal, window=window)
+                np.testing.assert_allclose(O, np.array(Ob), rtol=0, atol=1e-13)
+                np.testing.assert_allclose(L, np.array(Lb), rtol=0, atol=1e-13)
+
+
 ALL_PINS = [pin_brute, pin_library_sdpa, pin_causal_row0, pin_zero_query,
             pin_constant_values, pin_key_shift, pin_dominant_key, pin_grouped_heads,
-            pin_head_mapping_brute]
+            pin_head_mapping_brute, pin_window_library_sdpa, pin_window_closed_forms,
+            pin_window_brute]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -193,6 +244,16 @@ def test_online_recurrence_equals_batch(causal, blocks):
     Oo, Lo = oracle.attention_online_ref(q, k, v, 0.25, causal, blocks)
     np.testing.assert_allclose(Oo, O, rtol=0, atol=1e-12)
     np.testing.assert_allclose(Lo, L, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [(5, 5), (20, 0), (0, 30), (-1, 7)])
+def test_online_recurrence_equals_batch_with_window(window):
+    q, k, v = _rand(1, 2, 2, 120, 8, seed=23)
+    for causal in (False, True):
+        O, L = oracle.attention_ref(q, k, v, 0.25, causal, window=window)
+        Oo, Lo = oracle.attention_online_ref(q, k, v, 0.25, causal, [16, 9], window=window)
+        np.testing.assert_allclose(Oo, O, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Lo, L, rtol=0, atol=1e-12)
 
 
 def test_online_recurrence_growing_max():
@@ -280,13 +341,24 @@ def test_rejects_bad_heads():
 def _make_rows_fn(mistake):
     """A copy of the oracle's per-head step with one planted mistake."""
 
-    def rows_fn(qh, kh, vh, rows, scale, causal):
+    def rows_fn(qh, kh, vh, rows, scale, causal, window=None):
         T = kh.shape[0]
         kk, vv = (vh, kh) if mistake == "swap_kv" else (kh, vh)
         sc = 1.0 if mistake == "drop_scale" else scale
         s = (qh[rows] @ kk.T) * sc
         if mistake == "transpose_q":
             s = (qh[rows][:, ::-1] @ kk.T) * sc
+        if window is not None and mistake in ("window_off_by_one", "window_swapped"):
+            wl, wr = window if mistake == "window_off_by_one" else (window[1], window[0])
+            jj, ii = np.arange(T)[None, :], rows[:, None]
+            off = 1 if mistake == "window_off_by_one" else 0
+            wvalid = np.ones((len(rows), T), dtype=bool)
+            if wl >= 0:
+                wvalid &= jj >= ii - wl + off
+            if wr >= 0:
+                wvalid &= jj <= ii + wr
+        else:
+            wvalid = ar_mod.valid_keys(rows, T, False, window)
         if causal:
             if mistake == "strict_mask":
                 valid = np.arange(T)[None, :] < rows[:, None]
@@ -298,6 +370,7 @@ def _make_rows_fn(mistake):
                 valid = np.arange(T)[None, :] <= rows[:, None]
         else:
             valid = np.ones((len(rows), T), dtype=bool)
+        valid = valid & wvalid
         s = np.where(valid, s, -np.inf)
         m = s.max(axis=1)
         if mistake == "no_max_shift":
@@ -319,7 +392,7 @@ def _make_rows_fn(mistake):
 
 MISTAKES = ["swap_kv", "drop_scale", "transpose_q", "strict_mask", "loose_mask",
             "flipped_mask", "no_max_shift", "no_normalise", "log2_lse",
-            "lse_without_max", "head_modulo"]
+            "lse_without_max", "head_modulo", "window_off_by_one", "window_swapped"]
 
 
 @pytest.mark.parametrize("mistake", MISTAKES)
