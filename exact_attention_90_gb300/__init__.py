@@ -25,7 +25,7 @@ import os
 __all__ = [
     "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
-    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_split",
+    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_window", "fa_fwd_split",
     "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
@@ -57,6 +57,7 @@ EXPORTS = [
     ("fa_unit_qk", _I, [_P, _P, _P, _I, _P]),
     ("fa_unit_pv", _I, [_P, _P, _P, _P, _I, _I, ctypes.c_uint, ctypes.c_uint, _P]),
     ("fa_unit_timeout", _I, [ctypes.c_longlong, _P, _P]),
+    ("fa_fwd_window", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     ("fa_fwd_split", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
                           ctypes.c_ulonglong, _P]),
     ("fa_fwd_split_static", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
@@ -141,6 +142,15 @@ def fa_fwd_simt(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, stream=
                            _stream(stream))
 
 
+def fa_fwd_window(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, window_left, window_right, dtype,
+                  stream=None) -> int:
+    """The C function fa_fwd_window (band / sliding-window mask)."""
+    lib = load_library()
+    return lib.fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                             int(Hkv), int(T), int(d), float(scale), int(window_left),
+                             int(window_right), int(dtype), _stream(stream))
+
+
 def fa_fwd_split(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, num_splits,
                  workspace, workspace_bytes, stream=None) -> int:
     """The C function fa_fwd_split (split-KV forward into a caller workspace)."""
@@ -220,7 +230,7 @@ def _dtype_code(t) -> int:
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-        stream=None, kernel: str = "auto", num_splits: int | None = None):
+        stream=None, kernel: str = "auto", num_splits: int | None = None, window=None):
     """Attention forward on CUDA tensors; returns (o, lse).
 
     q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; all contiguous CUDA tensors of one
@@ -231,7 +241,9 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     picks the kernel by dtype.  ``num_splits`` splits every row block's keys
     that many ways (16-bit inputs; None = the library's heuristic, which
     splits only shapes too small to fill the GPU); the split path's
-    workspace is allocated with torch.  The call is asynchronous on
+    workspace is allocated with torch.  ``window = (wl, wr)`` restricts query
+    i to the keys i - wl <= j <= i + wr (-1: unbounded side), intersected with
+    the causal mask when ``causal`` is set.  The call is asynchronous on
     ``stream`` (default: the current torch stream).
     """
     import torch
@@ -256,6 +268,13 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
     if kernel not in ("auto", "simt"):
         raise ValueError("kernel must be 'auto' or 'simt'")
+    if window is not None:
+        wl, wr = (int(x) for x in window)
+        if causal:
+            wr = 0 if wr < 0 else min(wr, 0)
+        st = fa_fwd_window(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, wl, wr, code, stream)
+        _check(st, "fa_fwd_window")
+        return out, lse
     if kernel == "simt":
         st = fa_fwd_simt(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code,
                          stream)

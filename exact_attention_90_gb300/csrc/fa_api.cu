@@ -129,6 +129,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return dtype == FA_DTYPE_F32 ? fa::launch_simt(a) : fa::launch_tc(a);
 }
 
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int T, int d, float scale, int window_left,
+                        int window_right, fa_dtype dtype, void* stream) {
+  fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, T, d, scale, 0, dtype,
+                static_cast<cudaStream_t>(stream)};
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  a.window_left = window_left;
+  a.window_right = window_right;
+  fa_status s = fa::validate_fwd(a);
+  if (s != FA_OK) return s;
+  return dtype == FA_DTYPE_F32 ? fa::launch_simt(a) : fa::launch_tc(a);
+}
+
 fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int Hq, int Hkv, int T, int d, float scale, int causal, fa_dtype dtype,
                       void* stream) {

@@ -21,7 +21,18 @@ struct FwdArgs {
   int causal;
   fa_dtype dtype;
   cudaStream_t stream;
+  // band mask: keep key j for query i iff i - window_left <= j <= i + window_right
+  // (-1 = unbounded side); combined with `causal` by intersection
+  int window_left = -1;
+  int window_right = -1;
 };
+
+// The band the kernels apply: the window intersected with causal (j <= i).
+inline void effective_window(const FwdArgs& a, int& wl, int& wr) {
+  wl = a.window_left;
+  wr = a.window_right;
+  if (a.causal) wr = 0;  // min(wr, 0) for wr >= 0, and 0 for an unbounded wr
+}
 
 // Host-side argument checks shared by every entry point (no CUDA calls).
 fa_status validate_fwd(const FwdArgs& a);

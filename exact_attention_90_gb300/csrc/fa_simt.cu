@@ -137,11 +137,13 @@ __device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float* x, in
   }
 }
 
-template <typename Tin, int D, bool CAUSAL>
+// Band mask: keep key j for query i iff i - wl <= j <= i + wr (wl or wr < 0:
+// unbounded side); no mask is (-1, -1), causal attention (-1, 0).
+template <typename Tin, int D>
 __global__ void __launch_bounds__(128)
     fa_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                        const Tin* __restrict__ v, Tin* __restrict__ o, float* __restrict__ lse,
-                       int B, int Hq, int Hkv, int T, float scale) {
+                       int B, int Hq, int Hkv, int T, float scale, int wl, int wr) {
   using C = SimtCfg<D>;
   constexpr int QS = C::QS, PS = C::PS, OC = C::OC;
   constexpr int GW = D >= 64 ? 4 : (D == 32 ? 2 : 1);  // contiguous output columns
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(128)
   const int BH = B * Hq;
   const int n_qt = (T + BQ - 1) / BQ;
   const int n_kt = (T + BK - 1) / BK;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // longest blocks first
+  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // last (causal: longest) first
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int b = bh / Hq, h = bh - (bh / Hq) * Hq;
   const int hk = h / (Hq / Hkv);
@@ -175,8 +177,10 @@ __global__ void __launch_bounds__(128)
     for (int c = 0; c < OC; ++c) acc[i][c] = 0.f;
   }
 
-  const int n_kv = CAUSAL ? min(n_kt, (q0 + BQ - 1) / BK + 1) : n_kt;
-  for (int j = 0; j < n_kv; ++j) {
+  // KV blocks holding keys [q0 - wl, q0 + BQ - 1 + wr] of the band, within T
+  const int j_lo = wl < 0 ? 0 : max(0, q0 - wl) / BK;
+  const int j_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + BQ - 1 + wr) / BK + 1);
+  for (int j = j_lo; j < j_hi; ++j) {
     __syncthreads();  // previous block's K, V, P no longer in use
     load_tile<D, QS>(sK, k + kvoff, j * BK, T);
     load_tile<D, D>(sV, v + kvoff, j * BK, T);
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int key = kb + c;
-        keep[c] = key < T && (!CAUSAL || key <= row);
+        keep[c] = key < T && (wr < 0 || key <= row + wr) && (wl < 0 || key >= row - wl);
         if (keep[c]) mx = fmaxf(mx, s[i][c] * scale);
       }
 #pragma unroll
@@ -296,10 +300,10 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-template <typename Tin, int D, bool CAUSAL>
+template <typename Tin, int D>
 fa_status launch_simt_impl(const FwdArgs& a) {
   using C = SimtCfg<D>;
-  auto kern = fa_fwd_simt_kernel<Tin, D, CAUSAL>;
+  auto kern = fa_fwd_simt_kernel<Tin, D>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e =
@@ -308,20 +312,21 @@ fa_status launch_simt_impl(const FwdArgs& a) {
     attr_done = true;
   }
   const long long blocks = static_cast<long long>(a.B) * a.Hq * ((a.T + BQ - 1) / BQ);
+  int wl, wr;
+  effective_window(a, wl, wr);
   kern<<<static_cast<unsigned>(blocks), 128, C::SMEM_BYTES, a.stream>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
-      static_cast<Tin*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, a.scale);
+      static_cast<Tin*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, a.scale, wl, wr);
   return cuda_status(cudaGetLastError());
 }
 
 template <typename Tin>
 fa_status launch_simt_t(const FwdArgs& a) {
-  const bool c = a.causal != 0;
   switch (a.d) {
-    case 16: return c ? launch_simt_impl<Tin, 16, true>(a) : launch_simt_impl<Tin, 16, false>(a);
-    case 32: return c ? launch_simt_impl<Tin, 32, true>(a) : launch_simt_impl<Tin, 32, false>(a);
-    case 64: return c ? launch_simt_impl<Tin, 64, true>(a) : launch_simt_impl<Tin, 64, false>(a);
-    case 128: return c ? launch_simt_impl<Tin, 128, true>(a) : launch_simt_impl<Tin, 128, false>(a);
+    case 16: return launch_simt_impl<Tin, 16>(a);
+    case 32: return launch_simt_impl<Tin, 32>(a);
+    case 64: return launch_simt_impl<Tin, 64>(a);
+    case 128: return launch_simt_impl<Tin, 128>(a);
     default: return FA_ERR_UNSUPPORTED;
   }
 }

@@ -96,26 +96,35 @@ struct TcCfg : TcTile<D> {
 // log2 headroom of the lazy rescale: P values stay below 2^8
 #define FA_RESCALE_THRESHOLD 8.0f
 
-// KV tiles visited by the two 128-row Q tiles of row block qb (256 rows):
-// all tiles, or when causal those up to the diagonal; 0 for a tile past T.
-__host__ __device__ __forceinline__ void tc_tile_counts(int qb, int T, bool causal, int& n0,
-                                                        int& n1) {
-  const int n_all = (T + 127) >> 7;
-  const int qs0 = qb * 256, qs1 = qs0 + 128;
-  n0 = causal ? min(n_all, (qs0 >> 7) + 1) : n_all;
-  n1 = qs1 >= T ? 0 : (causal ? min(n_all, (qs1 >> 7) + 1) : n_all);
+// KV tiles [lo, hi) that the 128 query rows starting at qs need: the keys
+// [qs - wl, qs + 127 + wr] of the band mask (wl or wr < 0: unbounded side)
+// inside [0, T); no mask is (-1, -1), causal attention (-1, 0).  Empty
+// (lo = hi = 0) for rows past T.
+__host__ __device__ __forceinline__ void tc_tile_range(int qs, int T, int wl, int wr, int& lo,
+                                                       int& hi) {
+  if (qs >= T) {
+    lo = hi = 0;
+    return;
+  }
+  lo = wl < 0 ? 0 : max(0, qs - wl) >> 7;
+  const long long last =
+      wr < 0 ? static_cast<long long>(T) - 1
+             : min(static_cast<long long>(T) - 1, static_cast<long long>(qs) + 127 + wr);
+  hi = static_cast<int>(last >> 7) + 1;
 }
 
 // One work unit: 256 query rows [q0, q0 + 256) of (b, h) as two 128-row
 // tiles, over the KV tiles [j0, j0 + cnt) of split sp (of S).  Q tile t visits
-// c_t of them (0 when its KV range ends before j0); cnt = 0 marks an empty
-// split, which every role skips.
+// the local tiles [s_t, e_t) of them (s_t = e_t = 0: none); cnt = 0 marks an
+// empty split, which every role skips.  The two intervals overlap or touch
+// (a band keeps at least the diagonal key of every row), so every local tile
+// is visited by at least one Q tile.
 struct TcUnit {
-  int bh, b, hk, q0, sp, j0, c0, c1, cnt;
+  int bh, b, hk, q0, sp, j0, s0, e0, s1, e1, cnt;
 };
 
-template <bool CAUSAL>
-__device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T, int S) {
+__device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T, int S, int wl,
+                                          int wr) {
   TcUnit u;
   const int BH = B * Hq;
   const int n_qb = (T + 255) >> 8;
@@ -127,15 +136,26 @@ __device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T
   const int h = u.bh - u.b * Hq;
   u.hk = h / (Hq / Hkv);
   u.q0 = qb * 256;
-  int n0, n1;
-  tc_tile_counts(qb, T, CAUSAL, n0, n1);
-  const int nkv = max(n0, n1);
-  const int chunk = (nkv + S - 1) / S;  // KV tiles per split of this row block
-  u.j0 = u.sp * chunk;
-  const int j1 = min(nkv, u.j0 + chunk);
-  u.c0 = max(0, min(j1, n0) - u.j0);
-  u.c1 = max(0, min(j1, n1) - u.j0);
+  int lo0, hi0, lo1, hi1;
+  tc_tile_range(u.q0, T, wl, wr, lo0, hi0);
+  tc_tile_range(u.q0 + 128, T, wl, wr, lo1, hi1);
+  int ulo = lo0, uhi = hi0;
+  if (hi1 > lo1) {
+    ulo = min(ulo, lo1);
+    uhi = max(uhi, hi1);
+  }
+  const int chunk = (uhi - ulo + S - 1) / S;  // KV tiles per split of this row block
+  u.j0 = ulo + u.sp * chunk;
+  const int j1 = min(uhi, u.j0 + chunk);
   u.cnt = max(0, j1 - u.j0);
+  // with no left bound every row's keys start at key 0, so both tiles start
+  // at the split's first tile
+  u.s0 = wl < 0 ? 0 : max(0, lo0 - u.j0);
+  u.e0 = min(u.cnt, hi0 - u.j0);
+  if (u.e0 <= u.s0) u.s0 = u.e0 = 0;
+  u.s1 = wl < 0 ? 0 : max(0, lo1 - u.j0);
+  u.e1 = min(u.cnt, hi1 - u.j0);
+  if (u.e1 <= u.s1) u.s1 = u.e1 = 0;
   return u;
 }
 
@@ -146,15 +166,23 @@ __device__ __forceinline__ int tc_unit_index(int k) {
   return k * G + ((FA_TC_ZIGZAG && (k & 1)) ? G - 1 - bid : bid);
 }
 
+// Mask kinds, fixed at compile time so that the unmasked and causal kernels
+// carry no window arithmetic: no mask, causal (j <= i), or a band given by
+// the kernel's window arguments
+enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskBand = 2 };
+
 // F16: fp16 operands and output (else bf16); accumulation is fp32 either way
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
                      float* __restrict__ LSE, int B, int Hq, int Hkv, int T, float scale_log2,
                      int num_units, int S, float* __restrict__ part_o,
-                     float* __restrict__ part_lse) {
+                     float* __restrict__ part_lse, int window_left, int window_right) {
+  // the band [i - wl, i + wr] of the mask kind (a negative side: unbounded)
+  const int wl = MASK == kMaskBand ? window_left : -1;
+  const int wr = MASK == kMaskBand ? window_right : (MASK == kMaskCausal ? 0 : -1);
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
   constexpr int NSK = C::NSK, NSV = C::NSV;
@@ -263,7 +291,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
-          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T, S);
+          const TcUnit u = tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
           if (u.cnt == 0) continue;
           // Q of the previous unit is no longer read once its last S is done
           if (q_issued > 0 &&
@@ -327,11 +355,16 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
-          const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T, S);
+          const TcUnit u = tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
           if (u.cnt == 0) continue;
           if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
           ++nu;
           ptx::tc_fence_after();
+
+          // tile t is active at local KV tile j when s_t <= j < e_t
+          auto active = [&](int t, int j) {
+            return t == 0 ? (j >= u.s0 && j < u.e0) : (j >= u.s1 && j < u.e1);
+          };
 
           // S_t = Q_t K_j^T; on an abort no further MMA is issued (the ones in
           // flight are drained below)
@@ -349,15 +382,15 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                              Tile::DESC_HI, klo + Tile::kmajor_step(kk), Tile::DESC_HI, IDESC_QK,
                              kk > 0 ? 1u : 0u);
             ptx::mma_commit(&bar_sfull[t]);
-            // the last S of KV tile j releases its K stage (tile 1 is last when
-            // active); the unit's last S releases Q
-            if (t == 1 || j >= u.c1) ptx::mma_commit(&bar_kempty[st]);
-            if (j == u.cnt - 1 && (t == 1 || u.c1 < u.cnt)) ptx::mma_commit(bar_qempty);
+            // the last S of KV tile j releases its K stage (tile 1's, when
+            // active, comes after tile 0's); the unit's last S releases Q
+            if (t == 1 || !active(1, j)) ptx::mma_commit(&bar_kempty[st]);
+            if (j == u.cnt - 1 && (t == 1 || !active(1, j))) ptx::mma_commit(bar_qempty);
             return true;
           };
 
-          if (ok && u.c0 > 0) ok = issue_s(0, 0);
-          if (ok && u.c1 > 0) ok = issue_s(1, 0);
+          if (ok && active(0, 0)) ok = issue_s(0, 0);
+          if (ok && active(1, 0)) ok = issue_s(1, 0);
           for (int j = 0; ok && j < u.cnt; ++j) {
             const int c = vc + j;
             const int sv = c % NSV;
@@ -368,8 +401,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              const int nt = t == 0 ? u.c0 : u.c1;
-              if (ok && j < nt) {
+              if (ok && active(t, j)) {
                 int& pc = t == 0 ? pcnt0 : pcnt1;
                 if (!wait_bar(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
                   ok = false;
@@ -377,17 +409,27 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                 }
                 ++pc;
                 ptx::tc_fence_after();
+                const int first = t == 0 ? u.s0 : u.s1;
                 const uint32_t vlo = Tile::mnmajor_lo(aV + sv * TILE);
 #pragma unroll
                 for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
                   ptx::mma_ts_lh(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
                                  vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                                 (j > first || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(&bar_odone[t]);
-                const bool last_pv = (t == 1) || !(j < u.c1);
-                if (last_pv) ptx::mma_commit(&bar_vempty[sv]);
-                if (j + 1 < nt) ok = issue_s(t, j + 1);
+                if (t == 1 || !active(1, j)) ptx::mma_commit(&bar_vempty[sv]);
               }
+              if (ok && active(t, j + 1)) ok = issue_s(t, j + 1);
+            }
+            if (MASK == kMaskBand && ok && !active(0, j) && !active(1, j)) {
+              // a KV tile neither Q tile needs (a band keeps every row's
+              // diagonal key, so this does not occur): still release both
+              // stages once loaded, so the producer never waits on them
+              const int ck = kc + j;
+              ok = wait_bar(&bar_kfull[ck % NSK], (ck / NSK) & 1, abort_flag, &g_tc_err,
+                            kErrWaitMma);
+              ptx::mma_commit(&bar_kempty[ck % NSK]);
+              ptx::mma_commit(&bar_vempty[sv]);
             }
           }
           kc += u.cnt;
@@ -420,14 +462,16 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     for (int k = 0; ok; ++k) {
       const int idx = tc_unit_index(k);
       if (idx >= num_units) break;
-      const TcUnit u = tc_unit<CAUSAL>(idx, B, Hq, Hkv, T, S);
-      const int n = t == 0 ? u.c0 : u.c1;
+      const TcUnit u = tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
+      const int js = t == 0 ? u.s0 : u.s1;  // this Q tile's local KV tiles [js, je)
+      const int je = t == 0 ? u.e0 : u.e1;
+      const int n = je - js;
       const int q_start = u.q0 + 128 * t;
       const int grow = q_start + row;
       float m_ref = -INFINITY;
       float l = 0.f;
 
-      for (int j = 0; j < n; ++j, ++it) {
+      for (int j = js; j < je; ++j, ++it) {
         // warp-uniform decision: the tcgen05.ld/st below are warp-collective
         ok = __all_sync(0xffffffffu,
                         wait_bar(&bar_sfull[t], it & 1, abort_flag, &g_tc_err, kErrWaitSoftmax));
@@ -441,13 +485,17 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         // masked scores become -inf (+inf when scale < 0), so that their
         // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
         // never 0: the host passes the smallest normal float for scale = 0)
+        // a tile needs the mask unless all its keys lie in every row's band
+        // [row - wl, row + wr] and before T
         const int kb = (u.j0 + j) * 128;
-        const bool masked = (kb + 127 >= T) || (CAUSAL && kb + 127 > q_start);
-        if (masked) {
-          const int lim = CAUSAL ? min(T - 1, grow) - kb : T - 1 - kb;  // last kept column
+        const bool inside = kb + 127 < T && (wr < 0 || kb + 127 <= q_start + wr) &&
+                            (wl < 0 || kb >= q_start + 127 - wl);
+        if (!inside) {
+          const int hi_c = (wr < 0 ? T - 1 : min(T - 1, grow + wr)) - kb;  // last kept column
+          const int lo_c = wl < 0 ? -1 : grow - wl - kb;                     // first kept
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c > lim) s[c >> 5][c & 31] = __float_as_uint(mask_val);
+            if (c > hi_c || c < lo_c) s[c >> 5][c & 31] = __float_as_uint(mask_val);
         }
         // row maximum (minimum when scale < 0) with four independent chains
         float a[4];
@@ -503,7 +551,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         ptx::tmem_st64(tS, pall);
         // O correction (lazy, warp-uniform), before P is released: the next
         // P.V MMA accumulates into O
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        if (j > js && __any_sync(0xffffffffu, resc)) {
           if constexpr (D >= 32) {
 #pragma unroll
             for (int oc = 0; oc < D / 32; ++oc) {
@@ -641,27 +689,38 @@ static int tc_sm_count() {
 //   O = sum_s exp(L_s - L) O_s,
 // the same online-softmax rescaling, applied across splits instead of tiles.
 // Only the splits whose KV range reaches the row's tile are read.
-template <bool CAUSAL, bool F16>
+template <bool F16>
 __global__ void __launch_bounds__(256)
     fa_split_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                             uint16_t* __restrict__ O, float* __restrict__ LSE, int BH, int T,
-                            int D, int S) {
+                            int D, int S, int wl, int wr) {
   const long long rows = static_cast<long long>(BH) * T;
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int r = static_cast<int>(row % T);
-  int n0, n1;
-  tc_tile_counts(r >> 8, T, CAUSAL, n0, n1);
-  const int nkv = max(n0, n1);
-  const int nt = ((r >> 7) & 1) ? n1 : n0;
-  const int chunk = (nkv + S - 1) / S;
-  const int ns = min(S, (nt + chunk - 1) / chunk);  // splits that hold this row
+  // the row's KV tiles, the unit's union of both Q tiles' ranges, and the
+  // splits of that union (as the attention kernel cut them)
+  const int q0 = (r >> 8) << 8;
+  int lo0, hi0, lo1, hi1;
+  tc_tile_range(q0, T, wl, wr, lo0, hi0);
+  tc_tile_range(q0 + 128, T, wl, wr, lo1, hi1);
+  int ulo = lo0, uhi = hi0;
+  if (hi1 > lo1) {
+    ulo = min(ulo, lo1);
+    uhi = max(uhi, hi1);
+  }
+  const int chunk = (uhi - ulo + S - 1) / S;
+  const bool second = ((r >> 7) & 1) != 0;
+  const int rlo = second ? lo1 : lo0, rhi = second ? hi1 : hi0;
+  // splits [ulo + sp * chunk, ...) that hold part of [rlo, rhi)
+  const int sp_first = (rlo - ulo) / chunk;
+  const int ns = min(S, (rhi - ulo + chunk - 1) / chunk);
   float m = -INFINITY;
-  for (int sp = 0; sp < ns; ++sp) m = fmaxf(m, part_lse[sp * rows + row]);
+  for (int sp = sp_first; sp < ns; ++sp) m = fmaxf(m, part_lse[sp * rows + row]);
   float wsum = 0.f;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int sp = 0; sp < ns; ++sp) {
+  for (int sp = sp_first; sp < ns; ++sp) {
     const float w = expf(part_lse[sp * rows + row] - m);
     wsum += w;
     const float* po = part_o + (sp * rows + row) * D;
@@ -689,11 +748,11 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) LSE[row] = m + logf(wsum);
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, int MASK, bool F16>
 static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* part_lse) {
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
-  auto kern = fa_fwd_tc_kernel<D, CAUSAL, F16>;
+  auto kern = fa_fwd_tc_kernel<D, MASK, F16>;
   static bool attr_done = false;  // per instantiation; benign race (idempotent)
   if (!attr_done) {
     cudaError_t e =
@@ -725,34 +784,38 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
   // float stands in, and every finite score's exponent still rounds to 0
   float scale_log2 = a.scale * 1.4426950408889634f;
   if (scale_log2 == 0.f) scale_log2 = 1.17549435e-38f;
+  int wl, wr;
+  effective_window(a, wl, wr);
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, static_cast<uint16_t*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
-      static_cast<int>(units), S, S > 1 ? part_o : nullptr, S > 1 ? part_lse : nullptr);
+      static_cast<int>(units), S, S > 1 ? part_o : nullptr, S > 1 ? part_lse : nullptr, wl, wr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return cuda_status(e);
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.T;
-  fa_split_combine_kernel<CAUSAL, F16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0,
-                                         a.stream>>>(part_o, part_lse,
-                                                     static_cast<uint16_t*>(a.o), a.lse,
-                                                     a.B * a.Hq, a.T, D, S);
+  fa_split_combine_kernel<F16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0,
+                                 a.stream>>>(part_o, part_lse, static_cast<uint16_t*>(a.o), a.lse,
+                                             a.B * a.Hq, a.T, D, S, wl, wr);
   return cuda_status(cudaGetLastError());
+}
+
+template <int MASK, bool F16>
+static fa_status launch_tc_d(const FwdArgs& a, int S, float* po, float* pl) {
+  switch (a.d) {
+    case 16: return launch_tc_impl<16, MASK, F16>(a, S, po, pl);
+    case 32: return launch_tc_impl<32, MASK, F16>(a, S, po, pl);
+    case 64: return launch_tc_impl<64, MASK, F16>(a, S, po, pl);
+    case 128: return launch_tc_impl<128, MASK, F16>(a, S, po, pl);
+    default: return FA_ERR_UNSUPPORTED;
+  }
 }
 
 template <bool F16>
 static fa_status launch_tc_t(const FwdArgs& a, int S, float* po, float* pl) {
-  const bool c = a.causal != 0;
-  switch (a.d) {
-    case 16:
-      return c ? launch_tc_impl<16, true, F16>(a, S, po, pl) : launch_tc_impl<16, false, F16>(a, S, po, pl);
-    case 32:
-      return c ? launch_tc_impl<32, true, F16>(a, S, po, pl) : launch_tc_impl<32, false, F16>(a, S, po, pl);
-    case 64:
-      return c ? launch_tc_impl<64, true, F16>(a, S, po, pl) : launch_tc_impl<64, false, F16>(a, S, po, pl);
-    case 128:
-      return c ? launch_tc_impl<128, true, F16>(a, S, po, pl)
-               : launch_tc_impl<128, false, F16>(a, S, po, pl);
-    default: return FA_ERR_UNSUPPORTED;
-  }
+  int wl, wr;
+  effective_window(a, wl, wr);
+  if (wl < 0 && wr < 0) return launch_tc_d<kMaskNone, F16>(a, S, po, pl);
+  if (wl < 0 && wr == 0) return launch_tc_d<kMaskCausal, F16>(a, S, po, pl);
+  return launch_tc_d<kMaskBand, F16>(a, S, po, pl);
 }
 
 fa_status launch_tc(const FwdArgs& a) { return launch_tc_split(a, 1, nullptr, 0); }

@@ -77,6 +77,18 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int Hq, int Hkv, int T, int d, float scale, int causal,
                  fa_dtype dtype, void* stream);
 
+/* Band-masked (sliding-window) forward.  The yelogs.com Flash Attention2/
+ * Triton tutorial, section "1. 稀疏注意力支持" (sparse-attention support),
+ * restricts each query to the keys |i - j| <= window_size.  This call keeps
+ * key j for query i iff  i - window_left <= j <= i + window_right  (and
+ * j < T); -1 leaves that side unbounded.  The page's window is (w, w),
+ * causal attention is (-1, 0), no mask is (-1, -1).  KV tiles outside every
+ * row's band are skipped.  Other arguments, results and errors as fa_fwd
+ * (non-causal); FA_ERR_INVALID_ARG also for a window value below -1. */
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int Hq, int Hkv, int T, int d, float scale, int window_left,
+                        int window_right, fa_dtype dtype, void* stream);
+
 /* Split-KV forward (FlashDecoding-style; "Flash Attention Memory Optimization
  * Explained", section "Why It Matters", names FlashDecoding as the inference
  * extension).  Same operation, arguments and results as fa_fwd, for shapes

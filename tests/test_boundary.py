@@ -37,7 +37,7 @@ def test_headers_declare_the_abi():
     names = declared_functions()
     for n in ("fa_fwd", "fa_status_string", "fa_version", "fa_debug_sync_check",
               "fa_last_cuda_error", "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout",
-              "fa_fwd_simt", "fa_fwd_split", "fa_fwd_split_workspace_size",
+              "fa_fwd_simt", "fa_fwd_split", "fa_fwd_split_workspace_size", "fa_fwd_window",
               "fa_fwd_split_heuristic"):
         assert n in names
 
@@ -178,3 +178,19 @@ def test_split_rejects_bad_arguments_on_the_host(lib):
     assert split_call(ws=O) == fa.FA_ERR_INVALID_ARG        # workspace overlaps O
     assert split_call(q=0) == fa.FA_ERR_INVALID_ARG         # the fa_fwd checks apply too
     assert split_call(d=48) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_window_rejects_bad_arguments_on_the_host(lib):
+    a = dict(GOOD)
+
+    def wcall(wl, wr, **kw):
+        b = dict(a)
+        b.update(kw)
+        return fa.fa_fwd_window(b["q"], b["k"], b["v"], b["o"], b["lse"], b["B"], b["Hq"],
+                                b["Hkv"], b["T"], b["d"], b["scale"], wl, wr, b["dtype"], stream=0)
+
+    assert wcall(-2, 4) == fa.FA_ERR_INVALID_ARG
+    assert wcall(4, -5) == fa.FA_ERR_INVALID_ARG
+    assert wcall(4, 4, q=0) == fa.FA_ERR_INVALID_ARG
+    assert wcall(4, 4, d=24) == fa.FA_ERR_UNSUPPORTED
+    assert wcall(4, 4, o=O + 2) == fa.FA_ERR_MISALIGNED

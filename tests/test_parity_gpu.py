@@ -104,6 +104,43 @@ def test_full_parity_growing_row_max(cuda_lib, d, dtype):
         assert np.all(el <= bound), f"ramp d={d} {dtype}: max|dL|={el.max():.3g}"
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("window", [(0, 0), (3, 3), (64, 64), (100, 0), (0, 200), (-1, 50),
+                                    (300, -1), (127, 128), (2000, 2000)])
+@pytest.mark.parametrize("T,d", [(129, 32), (640, 128), (1000, 64)])
+def test_window_parity(cuda_lib, T, d, window, dtype):
+    """Band masks (the tutorial's sliding window |i - j| <= w and one-sided
+    bands) against the oracle, with ragged T and tiles skipped outside the
+    band."""
+    fa = cuda_lib
+    q, k, v = make_qkv(1, 4, 2, T, d, dtype=dtype, seed=T + d + window[0], device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd(q, k, v, scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+    O_ref, L_ref = oracle.attention_ref(q, k, v, scale, False, window=window)
+    tol_o, tol_l = TOL[dtype]
+    eo = float(np.max(np.abs(oracle.as_f64(o) - O_ref)))
+    el = float(np.max(np.abs(oracle.as_f64(lse) - L_ref)))
+    assert eo <= tol_o and el <= tol_l, f"window {window}: |dO|={eo:.3g} |dL|={el:.3g}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_window_causal_intersection(cuda_lib, dtype):
+    """causal + window (w, w) is the band (w, 0), and (-1, 0) is plain causal."""
+    fa = cuda_lib
+    q, k, v = make_qkv(2, 2, 2, 700, 128, dtype=dtype, seed=5, device="cuda")
+    o1, l1 = fa.fwd(q, k, v, causal=True, window=(90, 90))
+    o2, l2 = fa.fwd(q, k, v, window=(90, 0))
+    o3, l3 = fa.fwd(q, k, v, window=(-1, 0))
+    o4, l4 = fa.fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, 1 / math.sqrt(128), True, window=(90, 90))
+    assert float(np.max(np.abs(oracle.as_f64(o1) - O_ref))) <= TOL[dtype][0]
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("T,d,splits", [(1000, 128, 2), (1000, 64, 3), (777, 32, 5),
