@@ -22,12 +22,17 @@ Contents (each function cites the passage it follows):
 * ``attention_brute``    -- scalar pure-Python loops with ``math.fsum``, tiny
                             inputs only; an independent restatement used to pin
                             ``attention_ref``.
+* ``attention_bwd_ref``  -- the gradients of the forward with respect to Q, K
+                            and V for an upstream gradient dO, by the chain
+                            rule in fp64 (the backward oracle);
+                            ``attention_bwd_head_ref`` is its one-head step.
 * ``naive_score_bytes``  -- bytes of the T x T score matrix that the naive path
                             materialises (the pages' memory table).
 
 Parity status: every function above is pinned by ``tests/test_oracle.py``
 (closed forms, brute force, a library special case, invariants, and the pages'
-printed memory table).  Nothing here is "parity unpinned".
+printed memory table); the backward by ``tests/test_oracle_bwd.py`` (finite
+differences of the forward, torch autograd, invariants, closed forms).  Nothing here is "parity unpinned".
 """
 
 from .attention_ref import (
@@ -39,6 +44,7 @@ from .attention_ref import (
     naive_score_bytes,
     valid_keys,
 )
+from .attention_bwd_ref import attention_bwd_head_ref, attention_bwd_ref
 from .brute import attention_brute
 from .online_ref import attention_online_ref
 
@@ -49,6 +55,8 @@ __all__ = [
     "attention_probs_ref",
     "attention_online_ref",
     "attention_brute",
+    "attention_bwd_ref",
+    "attention_bwd_head_ref",
     "kv_head_of",
     "naive_score_bytes",
     "valid_keys",
