@@ -27,7 +27,8 @@ __all__ = [
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
     "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_window", "fa_fwd_split",
     "fa_fwd_split_static",
-    "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "FA_DTYPE_F32",
+    "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
+    "bwd", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
 
@@ -64,6 +65,9 @@ EXPORTS = [
     ("fa_fwd_split_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I]),
     ("fa_fwd_split_heuristic", _I, [_I, _I, _I, _I, _I, _I]),
     ("fa_fwd_simt", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I,
+                    _P, ctypes.c_ulonglong, _P]),
+    ("fa_bwd_workspace_size", ctypes.c_ulonglong, [_I, _I, _I]),
 ]
 
 
@@ -183,6 +187,20 @@ def fa_fwd_split_heuristic(B, Hq, Hkv, T, d, causal) -> int:
                                                  int(causal))
 
 
+def fa_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal, window_left,
+           window_right, dtype, workspace, workspace_bytes, stream=None) -> int:
+    """The C function fa_bwd (gradients of the forward for an upstream dO)."""
+    lib = load_library()
+    return lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq),
+                      _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(T), int(d), float(scale),
+                      int(causal), int(window_left), int(window_right), int(dtype),
+                      _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_workspace_size(B, Hq, T) -> int:
+    return load_library().fa_bwd_workspace_size(int(B), int(Hq), int(T))
+
+
 def fa_status_string(status: int) -> str:
     return load_library().fa_status_string(int(status)).decode()
 
@@ -294,3 +312,45 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         st = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code, stream)
         _check(st, "fa_fwd")
     return out, lse
+
+
+def bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None, window=None,
+        dq=None, dk=None, dv=None, stream=None):
+    """Attention backward on CUDA tensors; returns (dq, dk, dv).
+
+    q, k, v, o, lse are the forward's inputs and outputs (o and lse from a
+    forward with the same causal flag, scale and window); d_o is the upstream
+    gradient of o, like q.  dq, dk, dv may be given (shaped like q, k, v);
+    otherwise they are allocated with torch, as is the small workspace.  The
+    call is asynchronous on ``stream`` (default: the current torch stream).
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("d_o", d_o)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor [B, H, T, d]")
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have the dtype of q")
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(o.shape) != tuple(q.shape) or tuple(d_o.shape) != tuple(q.shape):
+        raise ValueError("o and d_o must be shaped like q")
+    if tuple(k.shape) != (B, Hkv, T, d) or tuple(v.shape) != (B, Hkv, T, d):
+        raise ValueError(f"k, v must be [B, Hkv, T, d]; got {tuple(k.shape)}, {tuple(v.shape)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, Hq, T] tensor")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    nbytes = fa_bwd_workspace_size(B, Hq, T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, int(bool(causal)), wl,
+                wr, code, ws, nbytes, stream)
+    _check(st, "fa_bwd")
+    return dq, dk, dv

@@ -21,8 +21,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_tc.cu", "fa_simt.cu", "fa_unit.cu", "fa_static.cu"]
-HEADERS = ["ptx.cuh", "tc_layout.cuh", "wait.cuh", "fa_internal.h"]
+SOURCES = ["fa_api.cu", "fa_tc.cu", "fa_simt.cu", "fa_unit.cu", "fa_static.cu", "fa_bwd_simt.cu",
+           "fa_bwd_tc.cu"]
+HEADERS = ["ptx.cuh", "tc_layout.cuh", "wait.cuh", "fa_internal.h", "simt_tiles.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

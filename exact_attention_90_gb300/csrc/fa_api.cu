@@ -111,7 +111,10 @@ fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word) {
   if (s != FA_OK) return s;
   s = unit_read_and_clear_error(&b);
   if (s != FA_OK) return s;
-  *word = a | b;
+  unsigned int c = 0;
+  s = bwd_read_and_clear_error(&c);
+  if (s != FA_OK) return s;
+  *word = a | b | c;
   return FA_OK;
 }
 
@@ -176,6 +179,50 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
       fa::overlap(workspace, need, lse, nl))
     return FA_ERR_INVALID_ARG;
   return fa::launch_tc_split(a, num_splits, workspace, workspace_bytes);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T,
+                 int d, float scale, int causal, int window_left, int window_right,
+                 fa_dtype dtype, void* workspace, unsigned long long workspace_bytes,
+                 void* stream) {
+  // the forward's checks cover q, k, v (as inputs), o and lse (as the
+  // "outputs" that must not overlap them) and every size
+  fa::FwdArgs f{q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, Hq, Hkv, T, d, scale,
+                causal, dtype, static_cast<cudaStream_t>(stream)};
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  fa_status s = fa::validate_fwd(f);
+  if (s != FA_OK) return s;
+  if (!d_o || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned16(d_o) || !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  if (workspace == nullptr) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
+  const size_t need = fa::bwd_workspace_bytes(B, Hq, T);
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const size_t e = dtype == FA_DTYPE_F32 ? 4 : 2;
+  const size_t nq = static_cast<size_t>(B) * Hq * T * d * e;
+  const size_t nkv = static_cast<size_t>(B) * Hkv * T * d * e;
+  const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+  // every written buffer (dq, dk, dv, workspace) against every other buffer
+  const void* bufs[10] = {q, k, v, o, lse, d_o, dq, dk, dv, workspace};
+  const size_t lens[10] = {nq, nkv, nkv, nq, nl, nq, nq, nkv, nkv, need};
+  for (int w = 6; w < 10; ++w)
+    for (int x = 0; x < 10; ++x)
+      if (x != w && fa::overlap(bufs[w], lens[w], bufs[x], lens[x])) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
+                window_left, window_right, dtype, static_cast<float*>(workspace),
+                static_cast<float*>(workspace) + static_cast<size_t>(B) * Hq *
+                                                     fa::bwd_rows_padded(T),
+                static_cast<cudaStream_t>(stream)};
+  s = fa::launch_bwd_prep(a);
+  if (s != FA_OK) return s;
+  return fa::bwd_tc_supported(a) ? fa::launch_bwd_tc(a) : fa::launch_bwd_simt(a);
+}
+
+unsigned long long fa_bwd_workspace_size(int B, int Hq, int T) {
+  if (B <= 0 || Hq <= 0 || T <= 0) return 0;
+  return fa::bwd_workspace_bytes(B, Hq, T);
 }
 
 unsigned long long fa_fwd_split_workspace_size(int B, int Hq, int T, int d, int num_splits) {

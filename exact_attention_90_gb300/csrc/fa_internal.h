@@ -63,6 +63,46 @@ int split_heuristic(int B, int Hq, int T, int causal);
 constexpr int kMaxSplits = 64;
 fa_status launch_simt(const FwdArgs& a);  // fp32, bf16 or fp16, CUDA cores
 
+// ------------------------------------------------------------- backward
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* d_o;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, Hq, Hkv, T, d;
+  float scale;
+  int causal;
+  int window_left, window_right;
+  fa_dtype dtype;
+  float* ws_delta;  // [B*Hq][Tp] D_i = sum_c dO[i][c] O[i][c] (0 on padded rows)
+  float* ws_lse2;   // [B*Hq][Tp] lse_i * log2(e) (+inf on padded rows)
+  cudaStream_t stream;
+};
+
+// Query rows per head in the workspace: T rounded up to a multiple of 128.
+inline int bwd_rows_padded(int T) { return (T + 127) / 128 * 128; }
+size_t bwd_workspace_bytes(int B, int Hq, int T);
+
+inline void effective_window(const BwdArgs& a, int& wl, int& wr) {
+  wl = a.window_left;
+  wr = a.window_right;
+  if (a.causal) wr = 0;
+}
+
+// D and lse * log2(e) into the workspace (CUDA cores; any dtype)
+fa_status launch_bwd_prep(const BwdArgs& a);
+// dQ, dK, dV with fp32 FFMA (any dtype and d)
+fa_status launch_bwd_simt(const BwdArgs& a);
+// dQ, dK, dV on the tensor cores (bf16 / fp16, d in {64, 128})
+fa_status launch_bwd_tc(const BwdArgs& a);
+bool bwd_tc_supported(const BwdArgs& a);
+fa_status bwd_read_and_clear_error(unsigned int* word);
+
 // Device error word shared by the kernels (read-and-clear, synchronous).
 fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
 

@@ -52,3 +52,14 @@ def make_structured_qkv(B: int, H: int, T: int, d: int, dtype: str = "bf16",
     k[..., 0] = torch.linspace(-ramp, ramp, T).expand(B, H, T) * (d ** 0.5)
     tdt = DTYPES[dtype]
     return tuple(x.to(tdt).contiguous().to(device) for x in (q, k, v))
+
+
+def make_grad_out(B: int, H: int, T: int, d: int, dtype: str = "bf16", seed: int = 0,
+                  device: str = "cpu"):
+    """An upstream gradient dO [B,H,T,d] for the backward pass: i.i.d. N(0, 1)
+    drawn in fp32 from a generator seeded with ``seed`` + 7919 (so that it is
+    not a copy of the Q drawn with the same seed), rounded to ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 7919)
+    x = torch.randn((B, H, T, d), generator=g, dtype=torch.float32)
+    return x.to(DTYPES[dtype]).contiguous().to(device)

@@ -143,6 +143,47 @@ unsigned long long fa_fwd_split_workspace_size(int B, int Hq, int T, int d, int 
  * on invalid sizes. */
 int fa_fwd_split_heuristic(int B, int Hq, int Hkv, int T, int d, int causal);
 
+/* Backward pass: gradients of o = attention(q, k, v) with respect to q, k and
+ * v for an upstream gradient d_o of o ("Flash Attention Memory Optimization
+ * Explained", section "Key Mechanisms", item "Backward Checkpointing": the
+ * forward's intermediates are recomputed, not stored).  The score matrix is
+ * rebuilt tile by tile from q, k and the forward's lse, P = exp(S - lse), and
+ *   dV  = sum over query heads of the group of P^T dO
+ *   dP  = dO V^T,   D_i = sum_c dO[i][c] * O[i][c]  (= sum_j P_ij dP_ij)
+ *   dS  = P * (dP - D)                              (softmax Jacobian)
+ *   dQ  = scale * dS K,   dK = sum over the group of scale * dS^T Q
+ * lse carries no gradient.
+ *   q, k, v, o, lse : the forward's inputs and outputs (o and lse exactly as
+ *                     a forward call with the same mask wrote them)
+ *   d_o   : [B][Hq][T][d] upstream gradient, element type `dtype`
+ *   dq    : [B][Hq][T][d], dk, dv : [B][Hkv][T][d]; written, element type
+ *           `dtype` (round-to-nearest-even from fp32 accumulation)
+ *   causal, window_left, window_right : the forward's mask (causal as
+ *           fa_fwd; the band as fa_fwd_window, -1 = unbounded side; both
+ *           combine by intersection)
+ *   workspace : DEVICE scratch of at least fa_bwd_workspace_size(B, Hq, T)
+ *           bytes, 16-byte aligned, not overlapping any other buffer; owned by
+ *           the caller; contents on entry ignored, on return undefined
+ * Kernels: bf16 and fp16 with d in {64, 128} run on the tensor cores (two
+ * kernels, one over KV tiles for dK and dV and one over query tiles for dQ,
+ * so that no gradient is accumulated by atomics: results are deterministic);
+ * fp32, and d in {16, 32}, run true-fp32 CUDA-core kernels.  All compute
+ * in fp32 after the input conversion.
+ * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG when an output (dq, dk, dv)
+ * overlaps another buffer or a window value is below -1, FA_ERR_WORKSPACE for
+ * a NULL or too small workspace.  Enqueues three kernels on `stream` and
+ * returns without synchronising. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T,
+                 int d, float scale, int causal, int window_left, int window_right,
+                 fa_dtype dtype, void* workspace, unsigned long long workspace_bytes,
+                 void* stream);
+
+/* Bytes of workspace fa_bwd needs: two fp32 values per query row (D_i and
+ * lse_i * log2(e)), rows padded to a multiple of 128 per head; 0 for invalid
+ * sizes. */
+unsigned long long fa_bwd_workspace_size(int B, int Hq, int T);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

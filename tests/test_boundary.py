@@ -38,7 +38,7 @@ def test_headers_declare_the_abi():
     for n in ("fa_fwd", "fa_status_string", "fa_version", "fa_debug_sync_check",
               "fa_last_cuda_error", "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout",
               "fa_fwd_simt", "fa_fwd_split", "fa_fwd_split_workspace_size", "fa_fwd_window",
-              "fa_fwd_split_heuristic"):
+              "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size"):
         assert n in names
 
 
@@ -194,3 +194,61 @@ def test_window_rejects_bad_arguments_on_the_host(lib):
     assert wcall(4, 4, q=0) == fa.FA_ERR_INVALID_ARG
     assert wcall(4, 4, d=24) == fa.FA_ERR_UNSUPPORTED
     assert wcall(4, 4, o=O + 2) == fa.FA_ERR_MISALIGNED
+
+
+DO, DQ, DK, DV, BWS = (BASE + ((7 + i) << 36) for i in range(5))
+
+
+def bwd_call(ws_bytes=None, **kw):
+    a = dict(GOOD, d_o=DO, dq=DQ, dk=DK, dv=DV, ws=BWS, wl=-1, wr=-1)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = fa.fa_bwd_workspace_size(a["B"], a["Hq"], a["T"])
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["d_o"], a["dq"], a["dk"],
+                     a["dv"], a["B"], a["Hq"], a["Hkv"], a["T"], a["d"], a["scale"], a["causal"],
+                     a["wl"], a["wr"], a["dtype"], a["ws"], ws_bytes, stream=0)
+
+
+def test_bwd_workspace_size(lib):
+    # two fp32 values per query row, rows padded to a multiple of 128 per head
+    assert fa.fa_bwd_workspace_size(2, 4, 100) == 2 * 2 * 4 * 128 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 128) == 2 * 128 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 129) == 2 * 256 * 4
+    assert fa.fa_bwd_workspace_size(0, 1, 10) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 0) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),            # the forward's checks apply
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d_o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=48), fa.FA_ERR_UNSUPPORTED),
+    (dict(Hq=4, Hkv=3), fa.FA_ERR_INVALID_ARG),
+    (dict(wl=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(wr=-3), fa.FA_ERR_INVALID_ARG),
+    (dict(d_o=DO + 8), fa.FA_ERR_MISALIGNED),
+    (dict(dk=DK + 2), fa.FA_ERR_MISALIGNED),
+    (dict(ws=0), fa.FA_ERR_WORKSPACE),
+    (dict(ws_bytes=100), fa.FA_ERR_WORKSPACE),
+    (dict(ws=BWS + 4), fa.FA_ERR_MISALIGNED),
+    (dict(dq=Q), fa.FA_ERR_INVALID_ARG),           # a gradient aliases an input
+    (dict(dk=DO + 4096), fa.FA_ERR_INVALID_ARG),   # dK overlaps dO
+    (dict(dv=DK), fa.FA_ERR_INVALID_ARG),          # two gradients alias
+    (dict(ws=DQ + 64), fa.FA_ERR_INVALID_ARG),     # the workspace overlaps dQ
+    (dict(ws=O), fa.FA_ERR_INVALID_ARG),           # the workspace overlaps O
+])
+def test_bwd_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert bwd_call(**kw) == status
+
+
+def test_bwd_tensor_api_refuses_cpu_tensors():
+    import torch
+
+    q = torch.zeros(1, 1, 8, 16)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(TypeError):
+        fa.bwd(q, q, q, q, lse, q)
