@@ -41,6 +41,7 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 fa_status validate_fwd(const FwdArgs& a) {
   if (!a.q || !a.k || !a.v || !a.o || !a.lse) return FA_ERR_INVALID_ARG;
   if (a.B <= 0 || a.Hq <= 0 || a.Hkv <= 0 || a.T <= 0 || a.d <= 0) return FA_ERR_INVALID_ARG;
+  if (a.T >= (1 << 30)) return FA_ERR_INVALID_ARG;  // band arithmetic stays in 32 bits
   if (a.Hq % a.Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(a.scale)) return FA_ERR_INVALID_ARG;
   if (a.causal != 0 && a.causal != 1) return FA_ERR_INVALID_ARG;
@@ -87,14 +88,14 @@ static void load_encode() {
 }
 
 CUresult make_tmap_16bit(CUtensorMap* map, const void* base, int d, int T, long long BH,
-                         int box_x, int swizzle, bool f16) {
+                         int box_x, int swizzle, bool f16, int box_rows) {
   std::call_once(g_encode_once, load_encode);
   if (g_encode_status != CUDA_SUCCESS) return g_encode_status;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), 128u, 1u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   return g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides,

@@ -28,10 +28,15 @@ struct FwdArgs {
 };
 
 // The band the kernels apply: the window intersected with causal (j <= i).
+// A side of T - 1 or more reaches every key, so it becomes unbounded (-1):
+// the kernels' band arithmetic then stays within a few T (T < 2^30).
+inline void band_of(int window_left, int window_right, int causal, int T, int& wl, int& wr) {
+  wl = window_left >= T - 1 ? -1 : window_left;
+  wr = window_right >= T - 1 ? -1 : window_right;
+  if (causal) wr = 0;  // min(wr, 0) for wr >= 0, and 0 for an unbounded wr
+}
 inline void effective_window(const FwdArgs& a, int& wl, int& wr) {
-  wl = a.window_left;
-  wr = a.window_right;
-  if (a.causal) wr = 0;  // min(wr, 0) for wr >= 0, and 0 for an unbounded wr
+  band_of(a.window_left, a.window_right, a.causal, a.T, wl, wr);
 }
 
 // Host-side argument checks shared by every entry point (no CUDA calls).
@@ -43,10 +48,10 @@ fa_status cuda_status(cudaError_t e);
 fa_status cu_status(CUresult r);
 
 // 3-D tensor map over a contiguous [BH][T][d] tensor of 16-bit elements
-// (fp16 when f16, else bf16) with boxes of box_x columns x 128 rows x 1 and
-// the given swizzle (CUtensorMapSwizzle).
+// (fp16 when f16, else bf16) with boxes of box_x columns x box_rows rows x 1
+// and the given swizzle (CUtensorMapSwizzle).
 CUresult make_tmap_16bit(CUtensorMap* map, const void* base, int d, int T, long long BH,
-                         int box_x, int swizzle, bool f16);
+                         int box_x, int swizzle, bool f16, int box_rows = 128);
 inline CUresult make_tmap_bf16(CUtensorMap* map, const void* base, int d, int T, long long BH,
                                int box_x, int swizzle) {
   return make_tmap_16bit(map, base, d, T, BH, box_x, swizzle, false);
@@ -89,9 +94,7 @@ inline int bwd_rows_padded(int T) { return (T + 127) / 128 * 128; }
 size_t bwd_workspace_bytes(int B, int Hq, int T);
 
 inline void effective_window(const BwdArgs& a, int& wl, int& wr) {
-  wl = a.window_left;
-  wr = a.window_right;
-  if (a.causal) wr = 0;
+  band_of(a.window_left, a.window_right, a.causal, a.T, wl, wr);
 }
 
 // D and lse * log2(e) into the workspace (CUDA cores; any dtype)

@@ -1,7 +1,8 @@
 // tc_layout.cuh -- tile geometry of the bf16 tensor-core attention kernel.
 //
-// One Q, K or V tile is 128 rows x d columns of bf16, brought into shared
-// memory by TMA as NBOX boxes of 128 rows x BOX_X columns, back to back.  The
+// One Q, K or V tile is ROWS (128, or 64 for the backward's query steps)
+// rows x d columns of bf16, brought into shared memory by TMA as NBOX boxes
+// of ROWS rows x BOX_X columns, back to back.  The
 // box row is BOX_X * 2 bytes (32, 64 or 128) and uses the swizzle of the same
 // width, so every 8-row group of a box is one swizzle atom of 8 * ROW_BYTES
 // bytes.  The same bytes serve
@@ -22,10 +23,11 @@
 
 namespace fa {
 
-template <int D>
+template <int D, int ROWS_ = 128>
 struct TcTile {
   static_assert(D == 16 || D == 32 || D == 64 || D == 128, "unsupported head dim");
-  static constexpr int ROWS = 128;
+  static_assert(ROWS_ == 128 || ROWS_ == 64, "tiles are 128 or 64 rows");
+  static constexpr int ROWS = ROWS_;
   static constexpr int BOX_X = D < 64 ? D : 64;
   static constexpr int ROW_BYTES = BOX_X * 2;
   static constexpr int NBOX = D / BOX_X;

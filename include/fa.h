@@ -53,7 +53,8 @@ typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null pointer, size <= 0, Hq % Hkv != 0,
                              non-finite scale, causal not 0/1, overlap of an
-                             output with another buffer, size overflow */
+                             output with another buffer, size overflow,
+                             T >= 2^30 */
   FA_ERR_UNSUPPORTED = 2, /* d not in {16,32,64,128} or unknown dtype */
   FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch etc.) */

@@ -100,6 +100,7 @@ def call(**kw):
     (dict(o=K + 4096), fa.FA_ERR_INVALID_ARG),   # output overlaps K
     (dict(lse=O + 64), fa.FA_ERR_INVALID_ARG),   # the two outputs overlap
     (dict(B=1 << 20, Hq=1 << 12, Hkv=1 << 12, T=1 << 20), fa.FA_ERR_INVALID_ARG),  # size overflow
+    (dict(B=1, Hq=1, Hkv=1, T=1 << 30), fa.FA_ERR_INVALID_ARG),  # T >= 2^30
 ])
 def test_fwd_rejects_bad_arguments_on_the_host(lib, kw, status):
     assert call(**kw) == status
