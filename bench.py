@@ -18,6 +18,12 @@ line (rank 0):
   cpu_baseline  the fp64 CPU oracle, as it stands, on a bounded sample of the
              same workload on this host's cores (rank 0, N=1 only)
 
+--pass bwd times the backward instead: one step = one fa_bwd call (row
+preparation, the dK/dV kernel and the dQ kernel) for an upstream gradient dO,
+O and LSE from one forward call before the timed region; flops = 2.5 x the
+forward's (the five T x T x d products S, dP, dV, dK, dQ; the kernels
+recompute S and dP a second time, which is not counted).
+
 --impl reference times that oracle alone, as the reference arm, with the same
 metric, unit and config.  Under torchrun (N > 1) every rank runs its own
 replica of the workload on its own GPU (no collective on the data path):
@@ -43,10 +49,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 BF16 dense peak"
+METRIC_BWD = ("attention bwd TFLOP/s (2.5x the causal-adjusted forward flops: S, dP, dV, dK, "
+              "dQ products) and % of GB300 BF16 dense peak")
+BWD_FLOP_FACTOR = 2.5
 UNIT = "TFLOP/s"
 L2_BYTES = 129e6
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["fa_tc.cu", "ptx.cuh", "tc_layout.cuh", "wait.cuh", "fa_simt.cu", "fa_api.cu"]
+# sources of the profiled forward kernel (device code and launch); an ncu
+# summary taken on other sources does not describe it
+KERNEL_SOURCES = ["fa_tc.cu", "ptx.cuh", "tc_layout.cuh", "wait.cuh"]
 
 
 # ---------------------------------------------------------------- helpers
@@ -286,7 +297,7 @@ def run_ours(args, w):
     import torch
 
     import exact_attention_90_gb300 as fa
-    from exact_attention_90_gb300.inputs import make_qkv
+    from exact_attention_90_gb300.inputs import make_grad_out, make_qkv
 
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
@@ -294,22 +305,36 @@ def run_ours(args, w):
     dist = init_dist(world, True)
     fa.load_library()  # raises if the CUDA library is missing: no fallback
 
+    bwd = args.pass_ == "bwd"
+    flops = w.flops * (BWD_FLOP_FACTOR if bwd else 1.0)
+    code = {"bf16": fa.FA_DTYPE_BF16, "f16": fa.FA_DTYPE_F16, "f32": fa.FA_DTYPE_F32}[w.dtype]
     qh, kh, vh = make_qkv(w.B, w.Hq, w.Hkv, w.T, w.d, dtype=w.dtype, seed=w.seed, mult=w.mult)
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
     in_bytes = sum(x.numel() * x.element_size() for x in (q, k, v))
-    flush = None if in_bytes > L2_BYTES else torch.empty(int(256e6), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if bwd:
+        doh = make_grad_out(w.B, w.Hq, w.T, w.d, dtype=w.dtype, seed=w.seed)
+        do = doh.to(dev)
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.T)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        in_bytes += 2 * o.numel() * o.element_size()
+    flush = None if in_bytes > L2_BYTES else torch.empty(int(256e6), dtype=torch.uint8, device=dev)
 
     def step():
         if flush is not None:
             flush.zero_()
-        st = fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.T, w.d, w.scale, int(w.causal),
-                       {"bf16": fa.FA_DTYPE_BF16, "f16": fa.FA_DTYPE_F16,
-                        "f32": fa.FA_DTYPE_F32}[w.dtype], stream)
+        if bwd:
+            st = fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.Hq, w.Hkv, w.T, w.d, w.scale,
+                           int(w.causal), -1, -1, code, ws, ws_bytes, stream)
+        else:
+            st = fa.fa_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.T, w.d, w.scale, int(w.causal),
+                           code, stream)
         if st != 0:
-            raise fa.FaError(st, "fa_fwd")
+            raise fa.FaError(st, "fa_bwd" if bwd else "fa_fwd")
 
     for _ in range(args.warmup):
         step()
@@ -346,23 +371,31 @@ def run_ours(args, w):
     sampler.stop()
     ms = e0.elapsed_time(e1)
     ms_max = reduce_max(dist, ms, dev)
-    value = aggregate(w.flops * args.steps, world, ms_max / 1e3)
+    value = aggregate(flops * args.steps, world, ms_max / 1e3)
     if fa.fa_debug_sync_check(stream) != 0:
         raise RuntimeError("kernel barrier wait timed out during the timed region")
 
-    # ---- end to end: pinned host inputs in, O and LSE out, every step
+    # ---- end to end: pinned host inputs in, outputs out, every step (forward:
+    # Q, K, V in, O and LSE out; backward: Q, K, V, O, LSE, dO in, dQ, dK, dV out)
     e2e_steps = max(3, min(args.steps, 50))
     qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
-    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    if bwd:
+        ins = [(q, qp), (k, kp), (v, vp), (o, o.cpu().pin_memory()),
+               (lse, lse.cpu().pin_memory()), (do, doh.pin_memory())]
+        outs = [(x, torch.empty(x.shape, dtype=x.dtype).pin_memory()) for x in (dq, dk, dv)]
+    else:
+        ins = [(q, qp), (k, kp), (v, vp)]
+        outs = [(x, torch.empty(x.shape, dtype=x.dtype).pin_memory()) for x in (o, lse)]
 
     def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
-        op.copy_(o, non_blocking=True)
-        lp.copy_(lse, non_blocking=True)
+        for dst, src in ins:
+            dst.copy_(src, non_blocking=True)
+        if bwd:
+            fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv)
+        else:
+            fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        for src, dst in outs:
+            dst.copy_(src, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -375,39 +408,44 @@ def run_ours(args, w):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
-    e2e_value = aggregate(w.flops * e2e_steps, world, e2e_ms / 1e3)
-    h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
-    d2h = op.numel() * op.element_size() + lp.numel() * lp.element_size()
+    e2e_value = aggregate(flops * e2e_steps, world, e2e_ms / 1e3)
+    h2d = sum(src.numel() * src.element_size() for _, src in ins)
+    d2h = sum(dst.numel() * dst.element_size() for _, dst in outs)
 
     peaks, src = load_peaks()
     ms_per = ms / args.steps
-    achieved = w.flops / (ms_per / 1e3) / 1e12
+    achieved = flops / (ms_per / 1e3) / 1e12
     # fp16 and bf16 share the dense tensor rate (nominal ratio 1:1); the fp32
     # kernel runs on the CUDA cores and has no tensor peak
     peak = float(peaks["bf16_tflops"]) if w.dtype in ("bf16", "f16") else None
-    traffic = ncu_traffic(w.name)
+    traffic = None if bwd else ncu_traffic(w.name)
     clocks = sampler.summary(t_wall0, t_wall1)
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q, K, V)",
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) Q, K, V" + (", dO)" if bwd else ")"),
         "config": config_of(w, world),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (3 if bwd else 1),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": (achieved / peak) if peak else None, "traffic": traffic,
                      "peak_source": f"bf16_tflops (burst) of {src}",
-                     "algorithmic_flops_per_launch": w.flops,
+                     "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes_per_launch": w.bytes,
                      "hbm_gbs": w.bytes / (ms_per / 1e3) / 1e9,
                      "hbm_frac": w.bytes / (ms_per / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
-                     "kernel": "fa_fwd_simt_kernel" if w.dtype == "f32" else "fa_fwd_tc_kernel"},
+                     "kernel": (("fa_bwd_prep_kernel + fa_bwd_dkdv_tc_kernel + fa_bwd_dq_tc_kernel "
+                                 "(one fa_bwd call)") if bwd else
+                                ("fa_fwd_simt_kernel" if w.dtype == "f32" else "fa_fwd_tc_kernel"))},
         "clocks": clocks,
     }
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if bwd:
+        line["config"]["pass"] = "backward"
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not bwd:
         os.environ.setdefault("OMP_NUM_THREADS", str(blas_threads()))
         cv, sample, _ = time_oracle(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": blas_threads(),
@@ -467,6 +505,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward (fa_bwd)")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--all", action="store_true", help="one line per workload shape")
     ap.add_argument("--filter", default="", help="with --all: substring of workload names")
