@@ -48,6 +48,12 @@ Readings of points the pages leave open or print inconsistently:
     when i - wl <= j <= i + wr, -1 meaning unbounded on that side; the page's
     window is (w, w), causal attention is (-1, 0), and `causal` combines with
     a window by intersection.
+  * local-global: the same passage keeps key j for query i when
+    |i - j| <= local_window OR j is one of the listed global tokens
+    (torch.isin over the key index): global tokens are keys every query
+    attends to.  The oracle takes global_tokens as a list of key indices;
+    entries outside [0, T) and repeats select nothing more (isin semantics);
+    with `causal` the union is intersected with j <= i.
   * MQA/GQA: [tri] "2. 多查詢注意力（MQA）" broadcasts a single KV head to all
     query heads; the grouped generalisation maps query head h to KV head
     h // (Hq // Hkv) (equivalently repeat_interleave of K, V along heads).
@@ -92,23 +98,30 @@ def _check_shapes(q, k, v):
     return B, Hq, Hkv, T, d
 
 
-def valid_keys(rows, T, causal, window=None):
-    """Boolean [len(rows), T]: key j is kept for query row i (the mask)."""
+def valid_keys(rows, T, causal, window=None, global_tokens=None):
+    """Boolean [len(rows), T]: key j is kept for query row i (the mask).
+
+    With ``global_tokens`` (the local-global mask of [tri] "1. 稀疏注意力支持")
+    the band ``window`` is the local part and the listed keys are kept for
+    every row as well: (band | isin(j, global_tokens)) & causal.
+    """
     j = np.arange(T)[None, :]
     i = np.asarray(rows)[:, None]
-    valid = np.ones((len(rows), T), dtype=bool)
-    if causal:
-        valid &= j <= i                               # keep j <= i
+    band = np.ones((len(rows), T), dtype=bool)
     if window is not None:
         wl, wr = window
         if wl >= 0:
-            valid &= j >= i - wl
+            band &= j >= i - wl
         if wr >= 0:
-            valid &= j <= i + wr
-    return valid
+            band &= j <= i + wr
+    if global_tokens is not None:
+        band |= np.isin(j, np.asarray(global_tokens, dtype=np.int64))
+    if causal:
+        band &= j <= i                                # keep j <= i
+    return band
 
 
-def _rows_of_head(qh, kh, vh, rows, scale, causal, window=None):
+def _rows_of_head(qh, kh, vh, rows, scale, causal, window=None, global_tokens=None):
     """The four naive steps for the query rows ``rows`` of one head (fp64).
 
     Step 1 (scores) and step 4 (weighted sum) are dense products; steps 2 and 3
@@ -118,7 +131,7 @@ def _rows_of_head(qh, kh, vh, rows, scale, causal, window=None):
     """
     T = kh.shape[0]
     s = (qh[rows] @ kh.T) * scale                     # step 1 + scale
-    valid = valid_keys(rows, T, causal, window)
+    valid = valid_keys(rows, T, causal, window, global_tokens)
     s = np.where(valid, s, -np.inf)                   # step 2: mask (excluded)
     m = s.max(axis=1)                                 # row maximum
     e = np.where(valid, np.exp(s - m[:, None]), 0.0)  # step 3: softmax numerator
@@ -128,7 +141,8 @@ def _rows_of_head(qh, kh, vh, rows, scale, causal, window=None):
     return o, lse, e / l[:, None]
 
 
-def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256, window=None):
+def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256, window=None,
+                  global_tokens=None):
     """Exact attention forward by its definition, fp64.
 
     Args:
@@ -140,6 +154,9 @@ def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256, win
       window: optional band (wl, wr): keep key j for query i iff
         i - wl <= j <= i + wr (-1 = unbounded side); every row must keep at
         least one key (true whenever wl, wr are -1 or >= 0).
+      global_tokens: optional key indices kept for every row in addition to
+        the band (the local-global mask; the page's local window is
+        window = (w, w)).
 
     Returns:
       (O, LSE): O [B, Hq, T, d] fp64, LSE [B, Hq, T] fp64 (natural log).
@@ -154,13 +171,14 @@ def attention_ref(q, k, v, scale: float, causal: bool, row_chunk: int = 256, win
             for r0 in range(0, T, row_chunk):
                 rows = np.arange(r0, min(T, r0 + row_chunk))
                 o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal,
-                                          window)
+                                          window, global_tokens)
                 O[b, h, rows] = o
                 L[b, h, rows] = lse
     return O, L
 
 
-def attention_rows_ref(q, k, v, scale: float, causal: bool, b: int, h: int, rows, window=None):
+def attention_rows_ref(q, k, v, scale: float, causal: bool, b: int, h: int, rows, window=None,
+                       global_tokens=None):
     """The definition evaluated for selected query rows of one (b, h) only.
 
     Used for parity at full workload sizes, where the whole oracle would take
@@ -175,11 +193,12 @@ def attention_rows_ref(q, k, v, scale: float, causal: bool, b: int, h: int, rows
     if rows.size and (rows.min() < 0 or rows.max() >= T):
         raise ValueError("row index out of range")
     hk = kv_head_of(h, Hq, Hkv)
-    o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal, window)
+    o, lse, _ = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal, window,
+                              global_tokens)
     return o, lse
 
 
-def attention_probs_ref(q, k, v, scale: float, causal: bool, window=None):
+def attention_probs_ref(q, k, v, scale: float, causal: bool, window=None, global_tokens=None):
     """The full probability matrix P [B, Hq, T, T] (fp64); small cases only."""
     q, k, v = as_f64(q), as_f64(k), as_f64(v)
     B, Hq, Hkv, T, d = _check_shapes(q, k, v)
@@ -188,7 +207,8 @@ def attention_probs_ref(q, k, v, scale: float, causal: bool, window=None):
     for b in range(B):
         for h in range(Hq):
             hk = kv_head_of(h, Hq, Hkv)
-            _, _, p = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal, window)
+            _, _, p = _rows_of_head(q[b, h], k[b, hk], v[b, hk], rows, scale, causal, window,
+                                    global_tokens)
             P[b, h] = p
     return P
 

@@ -30,11 +30,14 @@ def _to_nested(x):
     return x
 
 
-def attention_brute(q, k, v, scale: float, causal: bool, window=None):
+def attention_brute(q, k, v, scale: float, causal: bool, window=None, global_tokens=None):
     """Returns (O, LSE) as nested Python lists [B][Hq][T][d] and [B][Hq][T].
 
     window = (wl, wr) keeps, in addition, only keys i - wl <= j <= i + wr
     (-1 = unbounded side), the band form of the tutorial's sliding window.
+    global_tokens lists keys kept for every row in addition to that band (the
+    tutorial's local-global mask: band OR key in the list), still subject to
+    the causal rule.
     """
     q, k, v = _to_nested(q), _to_nested(k), _to_nested(v)
     B, Hq, T, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
@@ -52,7 +55,8 @@ def attention_brute(q, k, v, scale: float, causal: bool, window=None):
                 for j in range(T):
                     if causal and j > i:
                         continue
-                    if window is not None:
+                    is_global = global_tokens is not None and j in list(global_tokens)
+                    if window is not None and not is_global:
                         if window[0] >= 0 and j < i - window[0]:
                             continue
                         if window[1] >= 0 and j > i + window[1]:

@@ -219,10 +219,79 @@ def pin_window_brute(ref):
                 np.testing.assert_allclose(L, np.array(Lb), rtol=0, atol=1e-13)
 
 
+def _lg_mask(T, w, g, causal):
+    """The tutorial's local_global_mask written with torch ops: |i - j| <= w
+    OR torch.isin(j, global_tokens), then intersected with causal."""
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    keep = (i - j).abs() <= w
+    keep = keep | torch.isin(j, torch.tensor(g, dtype=torch.long))
+    if causal:
+        keep &= j <= i
+    return keep
+
+
+LG_CASES = ((40, 8, 3, [0], False), (40, 8, 2, [0, 1, 2, 3], True), (37, 16, 0, [5, 30], False),
+            (50, 4, 6, [49, 0, 17, 17, -3, 77], True), (33, 8, 1, [], False),
+            (45, 8, 4, list(range(0, 45, 7)), True))
+
+
+def pin_local_global_library_sdpa(ref):
+    """Local-global masks against torch's scaled_dot_product_attention (CPU,
+    float64) with the explicit mask of the tutorial's local_global_mask:
+    sinks at the start, tokens at the end, repeats and out-of-range entries
+    (selecting nothing), no global token, causal or not."""
+    for (T, d, w, g, causal) in LG_CASES:
+        q, k, v = _rand(1, 2, 2, T, d, seed=T + d + w)
+        O, L = ref(q, k, v, 0.4, causal, window=(w, w), global_tokens=g)
+        keep = _lg_mask(T, w, g, causal)
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        Ot = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=keep, scale=0.4)
+        np.testing.assert_allclose(O, Ot.numpy(), rtol=0, atol=1e-12)
+        sc = (torch.einsum("bhid,bhjd->bhij", tq, tk) * 0.4).masked_fill(~keep, float("-inf"))
+        np.testing.assert_allclose(L, torch.logsumexp(sc, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_local_global_brute(ref):
+    """Local-global masks against the scalar restatement on tiny shapes."""
+    for T in (4, 7):
+        for w, g in ((0, [0]), (1, [T - 1]), (0, [1, 1, 3])):
+            for causal in (False, True):
+                q, k, v = _rand(1, 2, 1, T, 3, seed=T * 13 + w + len(g))
+                O, L = ref(q, k, v, 0.7, causal, window=(w, w), global_tokens=g)
+                Ob, Lb = oracle.attention_brute(q, k, v, 0.7, causal, window=(w, w),
+                                                global_tokens=g)
+                np.testing.assert_allclose(O, np.array(Ob), rtol=0, atol=1e-13)
+                np.testing.assert_allclose(L, np.array(Lb), rtol=0, atol=1e-13)
+
+
+def pin_local_global_closed_forms(ref):
+    """Local window 0 with global token 0: row 0 sees only key 0 (O = V[0]);
+    row i > 0 sees exactly keys {0, i}, a two-way softmax; every key global
+    is no mask at all."""
+    T = 12
+    q, k, v = _rand(1, 1, 1, T, 4, seed=81)
+    O, L = ref(q, k, v, 0.5, True, window=(0, 0), global_tokens=[0])
+    np.testing.assert_array_equal(O[0, 0, 0], v[0, 0, 0])
+    for i in range(1, T):
+        s0 = 0.5 * q[0, 0, i] @ k[0, 0, 0]
+        si = 0.5 * q[0, 0, i] @ k[0, 0, i]
+        m = max(s0, si)
+        e0, ei = math.exp(s0 - m), math.exp(si - m)
+        np.testing.assert_allclose(O[0, 0, i], (e0 * v[0, 0, 0] + ei * v[0, 0, i]) / (e0 + ei),
+                                   rtol=0, atol=1e-13)
+        np.testing.assert_allclose(L[0, 0, i], m + math.log(e0 + ei), rtol=0, atol=1e-13)
+    O1, L1 = ref(q, k, v, 0.5, False, window=(0, 0), global_tokens=list(range(T)))
+    O2, L2 = ref(q, k, v, 0.5, False)
+    np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L1, L2, rtol=0, atol=1e-15)
+
+
 ALL_PINS = [pin_brute, pin_library_sdpa, pin_causal_row0, pin_zero_query,
             pin_constant_values, pin_key_shift, pin_dominant_key, pin_grouped_heads,
             pin_head_mapping_brute, pin_window_library_sdpa, pin_window_closed_forms,
-            pin_window_brute]
+            pin_window_brute, pin_local_global_library_sdpa, pin_local_global_brute,
+            pin_local_global_closed_forms]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -341,7 +410,7 @@ def test_rejects_bad_heads():
 def _make_rows_fn(mistake):
     """A copy of the oracle's per-head step with one planted mistake."""
 
-    def rows_fn(qh, kh, vh, rows, scale, causal, window=None):
+    def rows_fn(qh, kh, vh, rows, scale, causal, window=None, global_tokens=None):
         T = kh.shape[0]
         kk, vv = (vh, kh) if mistake == "swap_kv" else (kh, vh)
         sc = 1.0 if mistake == "drop_scale" else scale
@@ -359,6 +428,12 @@ def _make_rows_fn(mistake):
                 wvalid &= jj <= ii + wr
         else:
             wvalid = ar_mod.valid_keys(rows, T, False, window)
+        if global_tokens is not None:
+            g = np.asarray(global_tokens, dtype=np.int64)
+            if mistake == "global_as_queries":
+                wvalid = wvalid | np.isin(rows, g)[:, None]
+            elif mistake != "global_dropped":
+                wvalid = wvalid | np.isin(np.arange(T), g)[None, :]
         if causal:
             if mistake == "strict_mask":
                 valid = np.arange(T)[None, :] < rows[:, None]
@@ -371,6 +446,8 @@ def _make_rows_fn(mistake):
         else:
             valid = np.ones((len(rows), T), dtype=bool)
         valid = valid & wvalid
+        if mistake == "global_ignores_causal" and global_tokens is not None:
+            valid = valid | np.isin(np.arange(T), np.asarray(global_tokens))[None, :]
         s = np.where(valid, s, -np.inf)
         m = s.max(axis=1)
         if mistake == "no_max_shift":
@@ -392,7 +469,8 @@ def _make_rows_fn(mistake):
 
 MISTAKES = ["swap_kv", "drop_scale", "transpose_q", "strict_mask", "loose_mask",
             "flipped_mask", "no_max_shift", "no_normalise", "log2_lse",
-            "lse_without_max", "head_modulo", "window_off_by_one", "window_swapped"]
+            "lse_without_max", "head_modulo", "window_off_by_one", "window_swapped",
+            "global_dropped", "global_as_queries", "global_ignores_causal"]
 
 
 @pytest.mark.parametrize("mistake", MISTAKES)
