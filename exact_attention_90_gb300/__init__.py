@@ -28,6 +28,7 @@ __all__ = [
     "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_window", "fa_fwd_split",
     "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
+    "fa_fwd_local_global", "fa_fwd_local_global_workspace_size",
     "bwd", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
@@ -68,6 +69,9 @@ EXPORTS = [
     ("fa_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I,
                     _P, ctypes.c_ulonglong, _P]),
     ("fa_bwd_workspace_size", ctypes.c_ulonglong, [_I, _I, _I]),
+    ("fa_fwd_local_global", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _I, _I,
+                                 _P, ctypes.c_ulonglong, _P]),
+    ("fa_fwd_local_global_workspace_size", ctypes.c_ulonglong, [_I]),
 ]
 
 
@@ -197,6 +201,22 @@ def fa_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal, wi
                       _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def fa_fwd_local_global(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, local_window,
+                        global_tokens, num_global, dtype, workspace, workspace_bytes,
+                        stream=None) -> int:
+    """The C function fa_fwd_local_global (band OR global keys)."""
+    lib = load_library()
+    return lib.fa_fwd_local_global(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                   int(Hq), int(Hkv), int(T), int(d), float(scale), int(causal),
+                                   int(local_window), _ptr(global_tokens), int(num_global),
+                                   int(dtype), _ptr(workspace), int(workspace_bytes),
+                                   _stream(stream))
+
+
+def fa_fwd_local_global_workspace_size(T) -> int:
+    return load_library().fa_fwd_local_global_workspace_size(int(T))
+
+
 def fa_bwd_workspace_size(B, Hq, T) -> int:
     return load_library().fa_bwd_workspace_size(int(B), int(Hq), int(T))
 
@@ -248,7 +268,8 @@ def _dtype_code(t) -> int:
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-        stream=None, kernel: str = "auto", num_splits: int | None = None, window=None):
+        stream=None, kernel: str = "auto", num_splits: int | None = None, window=None,
+        global_tokens=None):
     """Attention forward on CUDA tensors; returns (o, lse).
 
     q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; all contiguous CUDA tensors of one
@@ -261,8 +282,11 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     splits only shapes too small to fill the GPU); the split path's
     workspace is allocated with torch.  ``window = (wl, wr)`` restricts query
     i to the keys i - wl <= j <= i + wr (-1: unbounded side), intersected with
-    the causal mask when ``causal`` is set.  The call is asynchronous on
-    ``stream`` (default: the current torch stream).
+    the causal mask when ``causal`` is set.  ``global_tokens`` (a CUDA int32
+    tensor of key indices) selects the local-global mask: ``window`` must
+    then be (w, w) or None (w = 0), and query i keeps key j when |i - j| <= w
+    or j is a global token (intersected with causal).  The call is
+    asynchronous on ``stream`` (default: the current torch stream).
     """
     import torch
 
@@ -286,6 +310,20 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
     if kernel not in ("auto", "simt"):
         raise ValueError("kernel must be 'auto' or 'simt'")
+    if global_tokens is not None:
+        wl, wr = (0, 0) if window is None else (int(window[0]), int(window[1]))
+        if wl != wr:
+            raise ValueError("the local-global mask takes a symmetric window (w, w)")
+        if (not isinstance(global_tokens, torch.Tensor) or not global_tokens.is_cuda
+                or global_tokens.dtype != torch.int32 or not global_tokens.is_contiguous()):
+            raise TypeError("global_tokens must be a contiguous CUDA int32 tensor")
+        nbytes = fa_fwd_local_global_workspace_size(T)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        st = fa_fwd_local_global(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), wl,
+                                 global_tokens if global_tokens.numel() else 0,
+                                 global_tokens.numel(), code, ws, nbytes, stream)
+        _check(st, "fa_fwd_local_global")
+        return out, lse
     if window is not None:
         wl, wr = (int(x) for x in window)
         if causal:

@@ -146,6 +146,45 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
   return dtype == FA_DTYPE_F32 ? fa::launch_simt(a) : fa::launch_tc(a);
 }
 
+fa_status fa_fwd_local_global(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                             int local_window, const int* global_tokens, int num_global,
+                             fa_dtype dtype, void* workspace, unsigned long long workspace_bytes,
+                             void* stream) {
+  fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype,
+                static_cast<cudaStream_t>(stream)};
+  if (local_window < 0 || num_global < 0) return FA_ERR_INVALID_ARG;
+  if (num_global > 0 && global_tokens == nullptr) return FA_ERR_INVALID_ARG;
+  a.window_left = local_window;
+  a.window_right = local_window;
+  fa_status s = fa::validate_fwd(a);
+  if (s != FA_OK) return s;
+  if (reinterpret_cast<uintptr_t>(global_tokens) & 3u) return FA_ERR_MISALIGNED;
+  if (workspace == nullptr) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
+  const size_t need = fa::lg_workspace_bytes(T);
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const size_t e = dtype == FA_DTYPE_F32 ? 4 : 2;
+  const size_t nq = static_cast<size_t>(B) * Hq * T * d * e;
+  const size_t nkv = static_cast<size_t>(B) * Hkv * T * d * e;
+  const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+  const size_t ng = static_cast<size_t>(num_global) * 4;
+  if (fa::overlap(workspace, need, q, nq) || fa::overlap(workspace, need, k, nkv) ||
+      fa::overlap(workspace, need, v, nkv) || fa::overlap(workspace, need, o, nq) ||
+      fa::overlap(workspace, need, lse, nl) ||
+      (ng > 0 && (fa::overlap(workspace, need, global_tokens, ng) ||
+                  fa::overlap(o, nq, global_tokens, ng) || fa::overlap(lse, nl, global_tokens, ng))))
+    return FA_ERR_INVALID_ARG;
+  s = fa::launch_lg_prep(a, global_tokens, num_global, workspace);
+  if (s != FA_OK) return s;
+  return dtype == FA_DTYPE_F32 ? fa::launch_simt(a) : fa::launch_tc(a);
+}
+
+unsigned long long fa_fwd_local_global_workspace_size(int T) {
+  if (T <= 0) return 0;
+  return fa::lg_workspace_bytes(T);
+}
+
 fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int Hq, int Hkv, int T, int d, float scale, int causal, fa_dtype dtype,
                       void* stream) {

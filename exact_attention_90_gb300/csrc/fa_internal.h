@@ -25,7 +25,24 @@ struct FwdArgs {
   // (-1 = unbounded side); combined with `causal` by intersection
   int window_left = -1;
   int window_right = -1;
+  // local-global mask (window_left = window_right = the local window): keys
+  // flagged in lg_bits are kept for every row as well, then causal applies.
+  // lg_bits: one bit per key, 4 words per 128-key tile; lg_list: the sorted
+  // tiles holding a flagged key, lg_count of them (written by launch_lg_prep)
+  bool local_global = false;
+  const uint32_t* lg_bits = nullptr;
+  const int* lg_list = nullptr;
+  const int* lg_count = nullptr;
 };
+
+// Workspace of the local-global mask for T keys: the key bitmask (16 bytes
+// per 128-key tile), the list of tiles holding a global key (4 bytes per
+// tile) and the list's length.
+size_t lg_workspace_bytes(int T);
+// Builds the bitmask and the tile list from `num_global` key indices (any
+// order; repeats and entries outside [0, T) select nothing more) into
+// `workspace` and points a.lg_* at them.
+fa_status launch_lg_prep(FwdArgs& a, const int* global_tokens, int num_global, void* workspace);
 
 // The band the kernels apply: the window intersected with causal (j <= i).
 // A side of T - 1 or more reaches every key, so it becomes unbounded (-1):

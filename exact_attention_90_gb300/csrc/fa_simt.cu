@@ -28,12 +28,15 @@ namespace {
 using namespace simt;
 
 // Band mask: keep key j for query i iff i - wl <= j <= i + wr (wl or wr < 0:
-// unbounded side); no mask is (-1, -1), causal attention (-1, 0).
+// unbounded side); no mask is (-1, -1), causal attention (-1, 0).  With
+// lg_bits (local-global mask: one bit per key) a flagged key is kept as well,
+// up to the row itself when lg_causal.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(128)
     fa_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                        const Tin* __restrict__ v, Tin* __restrict__ o, float* __restrict__ lse,
-                       int B, int Hq, int Hkv, int T, float scale, int wl, int wr) {
+                       int B, int Hq, int Hkv, int T, float scale, int wl, int wr,
+                       const uint32_t* __restrict__ lg_bits, int lg_causal) {
   using C = SimtCfg<D>;
   constexpr int QS = C::QS, PS = C::PS, OC = C::OC;
   constexpr int GW = D >= 64 ? 4 : (D == 32 ? 2 : 1);  // contiguous output columns
@@ -68,9 +71,16 @@ __global__ void __launch_bounds__(128)
   }
 
   // KV blocks holding keys [q0 - wl, q0 + BQ - 1 + wr] of the band, within T
-  const int j_lo = wl < 0 ? 0 : max(0, q0 - wl) / BK;
-  const int j_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + BQ - 1 + wr) / BK + 1);
+  const int b_lo = wl < 0 ? 0 : max(0, q0 - wl) / BK;
+  const int b_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + BQ - 1 + wr) / BK + 1);
+  // local-global: global keys may sit in any block (before the rows' last
+  // key when causal); blocks with neither band keys nor global keys are skipped
+  const int j_lo = lg_bits ? 0 : b_lo;
+  const int j_hi = lg_bits ? (lg_causal ? min(n_kt, min(T - 1, q0 + BQ - 1) / BK + 1) : n_kt)
+                           : b_hi;
   for (int j = j_lo; j < j_hi; ++j) {
+    if (lg_bits && (j < b_lo || j >= b_hi) && (__ldg(lg_bits + 2 * j) | __ldg(lg_bits + 2 * j + 1)) == 0u)
+      continue;
     __syncthreads();  // previous block's K, V, P no longer in use
     load_tile<D, QS>(sK, k + kvoff, j * BK, T);
     load_tile<D, D>(sV, v + kvoff, j * BK, T);
@@ -115,6 +125,8 @@ __global__ void __launch_bounds__(128)
       for (int c = 0; c < 4; ++c) {
         const int key = kb + c;
         keep[c] = key < T && (wr < 0 || key <= row + wr) && (wl < 0 || key >= row - wl);
+        if (lg_bits && !keep[c] && key < T && (!lg_causal || key <= row))
+          keep[c] = ((__ldg(lg_bits + (key >> 5)) >> (key & 31)) & 1u) != 0u;
         if (keep[c]) mx = fmaxf(mx, s[i][c] * scale);
       }
 #pragma unroll
@@ -206,7 +218,8 @@ fa_status launch_simt_impl(const FwdArgs& a) {
   effective_window(a, wl, wr);
   kern<<<static_cast<unsigned>(blocks), 128, C::SMEM_BYTES, a.stream>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
-      static_cast<Tin*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, a.scale, wl, wr);
+      static_cast<Tin*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, a.scale, wl, wr,
+      a.local_global ? a.lg_bits : nullptr, a.causal);
   return cuda_status(cudaGetLastError());
 }
 

@@ -121,6 +121,10 @@ __host__ __device__ __forceinline__ void tc_tile_range(int qs, int T, int wl, in
 // is visited by at least one Q tile.
 struct TcUnit {
   int bh, b, hk, q0, sp, j0, s0, e0, s1, e1, cnt;
+  // local-global masks: the unit's KV tiles are the nb global tiles below
+  // its band, the nband band tiles from j0 on, then the global tiles from
+  // list index ia on (below, j0 + j is the band's tile for nb = 0)
+  int nb, nband, ia;
 };
 
 __device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T, int S, int wl,
@@ -156,7 +160,65 @@ __device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T
   u.s1 = wl < 0 ? 0 : max(0, lo1 - u.j0);
   u.e1 = min(u.cnt, hi1 - u.j0);
   if (u.e1 <= u.s1) u.s1 = u.e1 = 0;
+  u.nb = 0;
+  u.nband = u.cnt;
+  u.ia = 0;
   return u;
+}
+
+// first index of the sorted list[0, n) whose entry is >= x (n if none)
+__device__ __forceinline__ int tc_lower_bound(const int* list, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(list + mid) < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// A unit of the local-global mask (no KV split): the union of both Q tiles'
+// bands [ulo, uhi) plus every tile holding a global key below ulo, or from
+// uhi up to the last tile any row of the unit may see (its own last row's
+// tile when causal).  Both Q tiles visit every tile of the unit; the mask
+// removes what a row does not see.
+__device__ __forceinline__ TcUnit tc_unit_lg(int idx, int B, int Hq, int Hkv, int T, int wl,
+                                             int wr, int causal, const int* glist,
+                                             const int* gcount) {
+  TcUnit u = tc_unit(idx, B, Hq, Hkv, T, 1, wl, wr);
+  const int ulo = u.j0, uhi = u.j0 + u.cnt;
+  const int n = __ldg(gcount);
+  const int cap = causal ? min(T - 1, u.q0 + 255) >> 7 : (T - 1) >> 7;
+  u.nb = tc_lower_bound(glist, n, ulo);
+  u.ia = tc_lower_bound(glist, n, uhi);
+  const int na = max(0, tc_lower_bound(glist, n, cap + 1) - u.ia);
+  u.nband = u.cnt;
+  u.cnt = u.nb + u.nband + na;
+  u.s0 = u.s1 = 0;
+  u.e0 = u.q0 < T ? u.cnt : 0;
+  u.e1 = u.q0 + 128 < T ? u.cnt : 0;
+  return u;
+}
+
+// Bits e of a 32-column group starting at column `base` with lo <= base + e <= hi.
+__device__ __forceinline__ uint32_t tc_range_bits(int lo, int hi, int base) {
+  const int a = max(lo - base, 0), b = min(hi - base, 31);
+  if (a > b) return 0u;
+  const uint32_t upto_b = b >= 31 ? 0xffffffffu : ((1u << (b + 1)) - 1u);
+  const uint32_t below_a = (1u << a) - 1u;  // a <= 31 here
+  return upto_b & ~below_a;
+}
+
+// KV tile of the unit's j-th visited tile
+template <bool LG>
+__device__ __forceinline__ int tc_tile_of(const TcUnit& u, int j, const int* glist) {
+  if constexpr (!LG) {
+    return u.j0 + j;
+  } else {
+    if (j < u.nb) return __ldg(glist + j);
+    if (j < u.nb + u.nband) return u.j0 + (j - u.nb);
+    return __ldg(glist + u.ia + (j - u.nb - u.nband));
+  }
 }
 
 // The k-th unit of this CTA: rounds of gridDim.x units, dealt forward on even
@@ -169,7 +231,7 @@ __device__ __forceinline__ int tc_unit_index(int k) {
 // Mask kinds, fixed at compile time so that the unmasked and causal kernels
 // carry no window arithmetic: no mask, causal (j <= i), or a band given by
 // the kernel's window arguments
-enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskBand = 2 };
+enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskBand = 2, kMaskLocalGlobal = 3 };
 
 // F16: fp16 operands and output (else bf16); accumulation is fp32 either way
 template <int D, int MASK, bool F16>
@@ -179,10 +241,17 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                      const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
                      float* __restrict__ LSE, int B, int Hq, int Hkv, int T, float scale_log2,
                      int num_units, int S, float* __restrict__ part_o,
-                     float* __restrict__ part_lse, int window_left, int window_right) {
+                     float* __restrict__ part_lse, int window_left, int window_right,
+                     const uint32_t* __restrict__ lg_bits, const int* __restrict__ lg_list,
+                     const int* __restrict__ lg_count, int lg_causal) {
+  constexpr bool LG = MASK == kMaskLocalGlobal;
   // the band [i - wl, i + wr] of the mask kind (a negative side: unbounded)
-  const int wl = MASK == kMaskBand ? window_left : -1;
-  const int wr = MASK == kMaskBand ? window_right : (MASK == kMaskCausal ? 0 : -1);
+  const int wl = (MASK == kMaskBand || LG) ? window_left : -1;
+  const int wr = (MASK == kMaskBand || LG) ? window_right : (MASK == kMaskCausal ? 0 : -1);
+  auto unit_at = [&](int idx) {
+    if constexpr (LG) return tc_unit_lg(idx, B, Hq, Hkv, T, wl, wr, lg_causal, lg_list, lg_count);
+    else return tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
+  };
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
   constexpr int NSK = C::NSK, NSV = C::NSV;
@@ -291,7 +360,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
-          const TcUnit u = tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
+          const TcUnit u = unit_at(idx);
           if (u.cnt == 0) continue;
           // Q of the previous unit is no longer read once its last S is done
           if (q_issued > 0 &&
@@ -306,7 +375,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
                                     u.q0 + 128 * t, u.bh, pol_q);
           ++q_issued;
           const int zkv = u.b * Hkv + u.hk;
-          for (int j = u.j0; j < u.j0 + u.cnt; ++j) {
+          for (int jj = 0; jj < u.cnt; ++jj) {
+            const int j = tc_tile_of<LG>(u, jj, lg_list);
             const int sk = kc % NSK, sv = vc % NSV;
             if (kc >= NSK && !wait_bar(&bar_kempty[sk], ((kc / NSK) - 1) & 1, abort_flag,
                                        &g_tc_err, kErrWaitLoad)) {
@@ -355,7 +425,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
-          const TcUnit u = tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
+          const TcUnit u = unit_at(idx);
           if (u.cnt == 0) continue;
           if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
           ++nu;
@@ -462,7 +532,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     for (int k = 0; ok; ++k) {
       const int idx = tc_unit_index(k);
       if (idx >= num_units) break;
-      const TcUnit u = tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
+      const TcUnit u = unit_at(idx);
       const int js = t == 0 ? u.s0 : u.s1;  // this Q tile's local KV tiles [js, je)
       const int je = t == 0 ? u.e0 : u.e1;
       const int n = je - js;
@@ -487,15 +557,31 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
         // never 0: the host passes the smallest normal float for scale = 0)
         // a tile needs the mask unless all its keys lie in every row's band
         // [row - wl, row + wr] and before T
-        const int kb = (u.j0 + j) * 128;
+        const int kb = tc_tile_of<LG>(u, j, lg_list) * 128;
         const bool inside = kb + 127 < T && (wr < 0 || kb + 127 <= q_start + wr) &&
                             (wl < 0 || kb >= q_start + 127 - wl);
         if (!inside) {
           const int hi_c = (wr < 0 ? T - 1 : min(T - 1, grow + wr)) - kb;  // last kept column
           const int lo_c = wl < 0 ? -1 : grow - wl - kb;                     // first kept
+          if constexpr (LG) {
+            // band OR a global key (before T, and not after the row when
+            // causal), as one keep word per 32 columns
+            const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(lg_bits) + (kb >> 7));
+            const int ghi_c = (lg_causal ? min(T - 1, grow) : T - 1) - kb;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > hi_c || c < lo_c) s[c >> 5][c & 31] = __float_as_uint(mask_val);
+            for (int g = 0; g < 4; ++g) {
+              const uint32_t gw = g == 0 ? g4.x : (g == 1 ? g4.y : (g == 2 ? g4.z : g4.w));
+              const uint32_t keep = tc_range_bits(lo_c, hi_c, 32 * g) |
+                                    (gw & tc_range_bits(0, ghi_c, 32 * g));
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > hi_c || c < lo_c) s[c >> 5][c & 31] = __float_as_uint(mask_val);
+          }
         }
         // row maximum (minimum when scale < 0) with four independent chains
         float a[4];
@@ -788,7 +874,8 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
   effective_window(a, wl, wr);
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, static_cast<uint16_t*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
-      static_cast<int>(units), S, S > 1 ? part_o : nullptr, S > 1 ? part_lse : nullptr, wl, wr);
+      static_cast<int>(units), S, S > 1 ? part_o : nullptr, S > 1 ? part_lse : nullptr, wl, wr,
+      a.lg_bits, a.lg_list, a.lg_count, a.causal);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return cuda_status(e);
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.T;
@@ -813,6 +900,7 @@ template <bool F16>
 static fa_status launch_tc_t(const FwdArgs& a, int S, float* po, float* pl) {
   int wl, wr;
   effective_window(a, wl, wr);
+  if (a.local_global) return launch_tc_d<kMaskLocalGlobal, F16>(a, S, po, pl);
   if (wl < 0 && wr < 0) return launch_tc_d<kMaskNone, F16>(a, S, po, pl);
   if (wl < 0 && wr == 0) return launch_tc_d<kMaskCausal, F16>(a, S, po, pl);
   return launch_tc_d<kMaskBand, F16>(a, S, po, pl);

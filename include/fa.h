@@ -90,6 +90,38 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
                         int B, int Hq, int Hkv, int T, int d, float scale, int window_left,
                         int window_right, fa_dtype dtype, void* stream);
 
+/* Local-global forward.  The yelogs.com Flash Attention2/Triton tutorial,
+ * section "1. 稀疏注意力支持" (sparse-attention support), defines the
+ * local-global mask: query i keeps key j iff |i - j| <= local_window OR j is
+ * one of the global tokens (torch.isin over the key index) -- global tokens are
+ * keys that every query attends to.  With causal = 1 the union is intersected
+ * with j <= i.  The KV tiles a query tile visits are those of its band plus
+ * the tiles holding a global key; all others are skipped.
+ *   local_window  : >= 0
+ *   global_tokens : DEVICE array of num_global int32 key indices, any order
+ *                   (4-byte aligned; may be NULL when num_global = 0); repeats
+ *                   and entries outside [0, T) select nothing more
+ *   workspace     : DEVICE scratch of at least
+ *                   fa_fwd_local_global_workspace_size(T) bytes, 16-byte
+ *                   aligned, not overlapping any other buffer; contents on
+ *                   entry ignored, on return undefined
+ * Other arguments and results as fa_fwd.  Enqueues a memset and three kernels
+ * (key bitmask, list of tiles holding global keys, attention).  Errors: as
+ * fa_fwd, plus FA_ERR_INVALID_ARG for local_window < 0, num_global < 0, a
+ * NULL global_tokens with num_global > 0 or an overlapping workspace;
+ * FA_ERR_MISALIGNED for a global_tokens pointer that is not 4-byte aligned;
+ * FA_ERR_WORKSPACE for a NULL or too small workspace. */
+fa_status fa_fwd_local_global(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                              int local_window, const int* global_tokens, int num_global,
+                              fa_dtype dtype, void* workspace,
+                              unsigned long long workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_fwd_local_global needs for T keys (a bitmask of the
+ * global keys and the list of 128-key tiles holding one: 20 bytes per tile,
+ * plus 16); 0 for T <= 0. */
+unsigned long long fa_fwd_local_global_workspace_size(int T);
+
 /* Split-KV forward (FlashDecoding-style; "Flash Attention Memory Optimization
  * Explained", section "Why It Matters", names FlashDecoding as the inference
  * extension).  Same operation, arguments and results as fa_fwd, for shapes

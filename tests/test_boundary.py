@@ -253,3 +253,37 @@ def test_bwd_tensor_api_refuses_cpu_tensors():
     lse = torch.zeros(1, 1, 8)
     with pytest.raises(TypeError):
         fa.bwd(q, q, q, q, lse, q)
+
+
+GT, LWS = BASE + (12 << 36), BASE + (13 << 36)
+
+
+def lg_call(w=3, gt=GT, n=5, ws=LWS, ws_bytes=None, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = fa.fa_fwd_local_global_workspace_size(a["T"])
+    return fa.fa_fwd_local_global(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"],
+                                  a["Hkv"], a["T"], a["d"], a["scale"], a["causal"], w, gt, n,
+                                  a["dtype"], ws, ws_bytes, stream=0)
+
+
+def test_local_global_workspace_size(lib):
+    # 16 bytes of key bits and 4 bytes of tile list per 128-key tile, plus 16
+    assert fa.fa_fwd_local_global_workspace_size(128) == 48
+    assert fa.fa_fwd_local_global_workspace_size(1000) == 8 * 20 + 16
+    assert fa.fa_fwd_local_global_workspace_size(0) == 0
+
+
+def test_local_global_rejects_bad_arguments_on_the_host(lib):
+    assert lg_call(w=-1) == fa.FA_ERR_INVALID_ARG
+    assert lg_call(n=-2) == fa.FA_ERR_INVALID_ARG
+    assert lg_call(gt=0, n=3) == fa.FA_ERR_INVALID_ARG
+    assert lg_call(gt=GT + 2) == fa.FA_ERR_MISALIGNED
+    assert lg_call(ws=0) == fa.FA_ERR_WORKSPACE
+    assert lg_call(ws_bytes=16) == fa.FA_ERR_WORKSPACE
+    assert lg_call(ws=LWS + 8) == fa.FA_ERR_MISALIGNED
+    assert lg_call(ws=O) == fa.FA_ERR_INVALID_ARG            # workspace overlaps O
+    assert lg_call(gt=O + 64) == fa.FA_ERR_INVALID_ARG       # tokens overlap an output
+    assert lg_call(q=0) == fa.FA_ERR_INVALID_ARG             # the fa_fwd checks apply
+    assert lg_call(d=40) == fa.FA_ERR_UNSUPPORTED
