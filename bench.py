@@ -462,34 +462,49 @@ def run_all(args):
     import torch
 
     import exact_attention_90_gb300 as fa
-    from exact_attention_90_gb300.inputs import make_qkv
+    from exact_attention_90_gb300.inputs import make_grad_out, make_qkv
     from exact_attention_90_gb300.workloads import all_workloads
 
     fa.load_library()
     peaks, src = load_peaks()
     dev = torch.device("cuda", 0)
     flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
+    bwd = args.pass_ == "bwd"
     for w in all_workloads():
         if args.filter and args.filter not in w.name:
             continue
         q, k, v = (x.to(dev) for x in make_qkv(w.B, w.Hq, w.Hkv, w.T, w.d, dtype=w.dtype,
                                                seed=w.seed, mult=w.mult))
         o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        if bwd:
+            do = make_grad_out(w.B, w.Hq, w.T, w.d, dtype=w.dtype, seed=w.seed).to(dev)
+            grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+
+            def call():
+                fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=grads[0],
+                       dk=grads[1], dv=grads[2])
+        else:
+            def call():
+                fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        call()
         torch.cuda.synchronize()
         times = []
         for _ in range(max(3, args.steps)):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            call()
             e1.record()
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
+        if fa.fa_debug_sync_check() != 0:
+            raise RuntimeError(f"{w.name}: kernel barrier wait timed out")
         ms = statistics.median(times)
-        tf = w.flops / (ms / 1e3) / 1e12
+        flops = w.flops * (BWD_FLOP_FACTOR if bwd else 1.0)
+        tf = flops / (ms / 1e3) / 1e12
         gbs = w.bytes / (ms / 1e3) / 1e9
-        print(json.dumps({"workload": w.name, "ms": ms, "tflops": tf,
-                          "frac_bf16_peak": tf / float(peaks["bf16_tflops"]),
+        print(json.dumps({"workload": w.name, "pass": "bwd" if bwd else "fwd", "ms": ms,
+                          "tflops": tf, "frac_bf16_peak": tf / float(peaks["bf16_tflops"]),
                           "hbm_gbs": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"]),
                           "peaks": src, "l2": "flushed (256 MB write) before each call"}),
               flush=True)

@@ -829,6 +829,8 @@ fa_status launch_bwd_tc_impl(const BwdArgs& a) {
 template <int MASK, bool F16>
 fa_status launch_bwd_tc_d(const BwdArgs& a) {
   switch (a.d) {
+    case 16: return launch_bwd_tc_impl<16, MASK, F16>(a);
+    case 32: return launch_bwd_tc_impl<32, MASK, F16>(a);
     case 64: return launch_bwd_tc_impl<64, MASK, F16>(a);
     case 128: return launch_bwd_tc_impl<128, MASK, F16>(a);
     default: return FA_ERR_UNSUPPORTED;
@@ -847,7 +849,7 @@ fa_status launch_bwd_tc_t(const BwdArgs& a) {
 }  // namespace
 
 bool bwd_tc_supported(const BwdArgs& a) {
-  return (a.dtype == FA_DTYPE_BF16 || a.dtype == FA_DTYPE_F16) && (a.d == 64 || a.d == 128);
+  return a.dtype == FA_DTYPE_BF16 || a.dtype == FA_DTYPE_F16;
 }
 
 fa_status launch_bwd_tc(const BwdArgs& a) {

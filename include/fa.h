@@ -197,11 +197,10 @@ int fa_fwd_split_heuristic(int B, int Hq, int Hkv, int T, int d, int causal);
  *   workspace : DEVICE scratch of at least fa_bwd_workspace_size(B, Hq, T)
  *           bytes, 16-byte aligned, not overlapping any other buffer; owned by
  *           the caller; contents on entry ignored, on return undefined
- * Kernels: bf16 and fp16 with d in {64, 128} run on the tensor cores (two
- * kernels, one over KV tiles for dK and dV and one over query tiles for dQ,
- * so that no gradient is accumulated by atomics: results are deterministic);
- * fp32, and d in {16, 32}, run true-fp32 CUDA-core kernels.  All compute
- * in fp32 after the input conversion.
+ * Kernels: bf16 and fp16 run on the tensor cores (two kernels, one over KV
+ * tiles for dK and dV and one over query tiles for dQ, so that no gradient is
+ * accumulated by atomics: results are deterministic); fp32 runs true-fp32
+ * CUDA-core kernels.  Accumulation is fp32 throughout.
  * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG when an output (dq, dk, dv)
  * overlaps another buffer or a window value is below -1, FA_ERR_WORKSPACE for
  * a NULL or too small workspace.  Enqueues three kernels on `stream` and
