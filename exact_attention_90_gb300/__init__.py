@@ -28,7 +28,8 @@ __all__ = [
     "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_window", "fa_fwd_split",
     "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
-    "fa_fwd_local_global", "fa_fwd_local_global_workspace_size",
+    "fa_fwd_local_global", "fa_fwd_local_global_workspace_size", "fa_bwd_local_global",
+    "fa_bwd_local_global_workspace_size",
     "bwd", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
@@ -72,6 +73,9 @@ EXPORTS = [
     ("fa_fwd_local_global", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _I, _I,
                                  _P, ctypes.c_ulonglong, _P]),
     ("fa_fwd_local_global_workspace_size", ctypes.c_ulonglong, [_I]),
+    ("fa_bwd_local_global", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
+                                 _I, _P, _I, _I, _P, ctypes.c_ulonglong, _P]),
+    ("fa_bwd_local_global_workspace_size", ctypes.c_ulonglong, [_I, _I, _I]),
 ]
 
 
@@ -217,6 +221,22 @@ def fa_fwd_local_global_workspace_size(T) -> int:
     return load_library().fa_fwd_local_global_workspace_size(int(T))
 
 
+def fa_bwd_local_global(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
+                        local_window, global_tokens, num_global, dtype, workspace,
+                        workspace_bytes, stream=None) -> int:
+    """The C function fa_bwd_local_global."""
+    lib = load_library()
+    return lib.fa_bwd_local_global(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(T),
+                                   int(d), float(scale), int(causal), int(local_window),
+                                   _ptr(global_tokens), int(num_global), int(dtype),
+                                   _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_local_global_workspace_size(B, Hq, T) -> int:
+    return load_library().fa_bwd_local_global_workspace_size(int(B), int(Hq), int(T))
+
+
 def fa_bwd_workspace_size(B, Hq, T) -> int:
     return load_library().fa_bwd_workspace_size(int(B), int(Hq), int(T))
 
@@ -353,14 +373,15 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
 
 
 def bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None, window=None,
-        dq=None, dk=None, dv=None, stream=None):
+        dq=None, dk=None, dv=None, stream=None, global_tokens=None):
     """Attention backward on CUDA tensors; returns (dq, dk, dv).
 
     q, k, v, o, lse are the forward's inputs and outputs (o and lse from a
     forward with the same causal flag, scale and window); d_o is the upstream
     gradient of o, like q.  dq, dk, dv may be given (shaped like q, k, v);
-    otherwise they are allocated with torch, as is the small workspace.  The
-    call is asynchronous on ``stream`` (default: the current torch stream).
+    otherwise they are allocated with torch, as is the small workspace.
+    ``global_tokens`` selects the local-global mask as in ``fwd``.  The call
+    is asynchronous on ``stream`` (default: the current torch stream).
     """
     import torch
 
@@ -385,6 +406,21 @@ def bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if global_tokens is not None:
+        wl, wr = (0, 0) if window is None else (int(window[0]), int(window[1]))
+        if wl != wr:
+            raise ValueError("the local-global mask takes a symmetric window (w, w)")
+        if (not isinstance(global_tokens, torch.Tensor) or not global_tokens.is_cuda
+                or global_tokens.dtype != torch.int32 or not global_tokens.is_contiguous()):
+            raise TypeError("global_tokens must be a contiguous CUDA int32 tensor")
+        nbytes = fa_bwd_local_global_workspace_size(B, Hq, T)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        st = fa_bwd_local_global(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale,
+                                 int(bool(causal)), wl,
+                                 global_tokens if global_tokens.numel() else 0,
+                                 global_tokens.numel(), code, ws, nbytes, stream)
+        _check(st, "fa_bwd_local_global")
+        return dq, dk, dv
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     nbytes = fa_bwd_workspace_size(B, Hq, T)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)

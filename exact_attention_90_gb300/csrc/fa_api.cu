@@ -221,43 +221,98 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
   return fa::launch_tc_split(a, num_splits, workspace, workspace_bytes);
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                 const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T,
-                 int d, float scale, int causal, int window_left, int window_right,
-                 fa_dtype dtype, void* workspace, unsigned long long workspace_bytes,
-                 void* stream) {
+}  // extern "C"
+
+namespace fa {
+
+// The backward entry points: checks, then the row preparation and the
+// gradient kernels.  With lg_tokens >= 0 (local-global mask; the window is
+// the local window on both sides) the key sets are built in the workspace
+// after the rows' part.
+static fa_status bwd_entry(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* d_o, void* dq, void* dk, void* dv, int B,
+                           int Hq, int Hkv, int T, int d, float scale, int causal,
+                           int window_left, int window_right, const int* lg_tokens,
+                           int lg_num, fa_dtype dtype, void* workspace,
+                           unsigned long long workspace_bytes, void* stream) {
   // the forward's checks cover q, k, v (as inputs), o and lse (as the
   // "outputs" that must not overlap them) and every size
-  fa::FwdArgs f{q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, Hq, Hkv, T, d, scale,
-                causal, dtype, static_cast<cudaStream_t>(stream)};
+  FwdArgs f{q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, Hq, Hkv, T, d, scale,
+            causal, dtype, static_cast<cudaStream_t>(stream)};
   if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
-  fa_status s = fa::validate_fwd(f);
+  fa_status s = validate_fwd(f);
   if (s != FA_OK) return s;
   if (!d_o || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!fa::aligned16(d_o) || !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv))
+  if (!aligned16(d_o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
+  const bool lg = lg_num >= 0;
+  if (lg && lg_num > 0 && lg_tokens == nullptr) return FA_ERR_INVALID_ARG;
+  if (lg && (reinterpret_cast<uintptr_t>(lg_tokens) & 3u)) return FA_ERR_MISALIGNED;
   if (workspace == nullptr) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
-  const size_t need = fa::bwd_workspace_bytes(B, Hq, T);
+  const size_t rows_bytes = bwd_workspace_bytes(B, Hq, T);
+  const size_t need = rows_bytes + (lg ? lg_workspace_bytes(T) : 0);
   if (workspace_bytes < need) return FA_ERR_WORKSPACE;
   const size_t e = dtype == FA_DTYPE_F32 ? 4 : 2;
   const size_t nq = static_cast<size_t>(B) * Hq * T * d * e;
   const size_t nkv = static_cast<size_t>(B) * Hkv * T * d * e;
   const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+  const size_t ng = lg ? static_cast<size_t>(lg_num) * 4 : 0;
   // every written buffer (dq, dk, dv, workspace) against every other buffer
-  const void* bufs[10] = {q, k, v, o, lse, d_o, dq, dk, dv, workspace};
-  const size_t lens[10] = {nq, nkv, nkv, nq, nl, nq, nq, nkv, nkv, need};
-  for (int w = 6; w < 10; ++w)
-    for (int x = 0; x < 10; ++x)
-      if (x != w && fa::overlap(bufs[w], lens[w], bufs[x], lens[x])) return FA_ERR_INVALID_ARG;
-  fa::BwdArgs a{q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
-                window_left, window_right, dtype, static_cast<float*>(workspace),
-                static_cast<float*>(workspace) + static_cast<size_t>(B) * Hq *
-                                                     fa::bwd_rows_padded(T),
-                static_cast<cudaStream_t>(stream)};
-  s = fa::launch_bwd_prep(a);
+  const void* bufs[11] = {q, k, v, o, lse, d_o, lg_tokens, dq, dk, dv, workspace};
+  const size_t lens[11] = {nq, nkv, nkv, nq, nl, nq, ng, nq, nkv, nkv, need};
+  for (int w = 7; w < 11; ++w)
+    for (int x = 0; x < 11; ++x)
+      if (x != w && lens[x] > 0 && overlap(bufs[w], lens[w], bufs[x], lens[x]))
+        return FA_ERR_INVALID_ARG;
+  BwdArgs a{q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
+            window_left, window_right, dtype, static_cast<float*>(workspace),
+            static_cast<float*>(workspace) + static_cast<size_t>(B) * Hq * bwd_rows_padded(T),
+            static_cast<cudaStream_t>(stream)};
+  if (lg) {
+    LgSets g;
+    s = lg_prep(T, lg_tokens, lg_num, static_cast<uint8_t*>(workspace) + rows_bytes, a.stream,
+                &g);
+    if (s != FA_OK) return s;
+    a.local_global = true;
+    a.lg_bits = g.bits;
+    a.lg_list = g.list;
+    a.lg_count = g.count;
+  }
+  s = launch_bwd_prep(a);
   if (s != FA_OK) return s;
-  return fa::bwd_tc_supported(a) ? fa::launch_bwd_tc(a) : fa::launch_bwd_simt(a);
+  return bwd_tc_supported(a) ? launch_bwd_tc(a) : launch_bwd_simt(a);
+}
+
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T,
+                 int d, float scale, int causal, int window_left, int window_right,
+                 fa_dtype dtype, void* workspace, unsigned long long workspace_bytes,
+                 void* stream) {
+  return fa::bwd_entry(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
+                       window_left, window_right, nullptr, -1, dtype, workspace,
+                       workspace_bytes, stream);
+}
+
+fa_status fa_bwd_local_global(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                              int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                              int local_window, const int* global_tokens, int num_global,
+                              fa_dtype dtype, void* workspace,
+                              unsigned long long workspace_bytes, void* stream) {
+  if (local_window < 0 || num_global < 0) return FA_ERR_INVALID_ARG;
+  return fa::bwd_entry(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
+                       local_window, local_window, global_tokens, num_global, dtype, workspace,
+                       workspace_bytes, stream);
+}
+
+unsigned long long fa_bwd_local_global_workspace_size(int B, int Hq, int T) {
+  if (B <= 0 || Hq <= 0 || T <= 0) return 0;
+  return fa::bwd_workspace_bytes(B, Hq, T) + fa::lg_workspace_bytes(T);
 }
 
 unsigned long long fa_bwd_workspace_size(int B, int Hq, int T) {

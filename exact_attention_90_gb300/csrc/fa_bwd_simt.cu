@@ -70,9 +70,20 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// keep key j for query i: inside [0, T) and the band i - wl <= j <= i + wr
-__device__ __forceinline__ bool band_keep(int i, int j, int T, int wl, int wr) {
-  return i < T && j < T && (wr < 0 || j <= i + wr) && (wl < 0 || j >= i - wl);
+// keep key j for query i: inside [0, T) and the band i - wl <= j <= i + wr,
+// or (local-global masks, lg_bits != nullptr) j is a global key, not after i
+// when lg_causal
+__device__ __forceinline__ bool band_keep(int i, int j, int T, int wl, int wr,
+                                          const uint32_t* lg_bits = nullptr, int lg_causal = 0) {
+  if (i >= T || j >= T) return false;
+  if ((wr < 0 || j <= i + wr) && (wl < 0 || j >= i - wl)) return true;
+  return lg_bits != nullptr && (!lg_causal || j <= i) &&
+         ((__ldg(lg_bits + (j >> 5)) >> (j & 31)) & 1u) != 0u;
+}
+
+// any global key in the 64-key block kb0 .. kb0 + 63 (two bitmask words)
+__device__ __forceinline__ bool block_has_global(const uint32_t* lg_bits, int kb0) {
+  return (__ldg(lg_bits + (kb0 >> 5)) | __ldg(lg_bits + (kb0 >> 5) + 1)) != 0u;
 }
 
 // acc[8][OC] += A[rows ty*8.., 0..63] (stride PS) x B[0..63][cols] (stride BS)
@@ -184,7 +195,8 @@ __global__ void __launch_bounds__(128)
                           const Tin* __restrict__ v, const Tin* __restrict__ d_o,
                           const float* __restrict__ delta, const float* __restrict__ lse2,
                           Tin* __restrict__ dq, int B, int Hq, int Hkv, int T, int Tp,
-                          float scale, int wl, int wr) {
+                          float scale, int wl, int wr, const uint32_t* __restrict__ lg_bits,
+                          int lg_causal) {
   constexpr int QS = SimtCfg<D>::QS, PS = SimtCfg<D>::PS, OC = SimtCfg<D>::OC;
   extern __shared__ float4 smem4[];
   float* sQ = reinterpret_cast<float*>(smem4);
@@ -220,9 +232,14 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int c = 0; c < OC; ++c) acc[i][c] = 0.f;
 
-  const int j_lo = wl < 0 ? 0 : max(0, q0 - wl) / 64;
-  const int j_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + 63 + wr) / 64 + 1);
+  const int b_lo = wl < 0 ? 0 : max(0, q0 - wl) / 64;
+  const int b_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + 63 + wr) / 64 + 1);
+  // local-global: any block may hold global keys (up to the rows' last key
+  // when causal); blocks with neither band keys nor global keys are skipped
+  const int j_lo = lg_bits ? 0 : b_lo;
+  const int j_hi = lg_bits ? (lg_causal ? min(n_kt, min(T - 1, q0 + 63) / 64 + 1) : n_kt) : b_hi;
   for (int j = j_lo; j < j_hi; ++j) {
+    if (lg_bits && (j < b_lo || j >= b_hi) && !block_has_global(lg_bits, j * 64)) continue;
     __syncthreads();  // previous block's K, V and dS no longer in use
     load_tile<D, QS>(sK, k + kvoff, j * 64, T);
     load_tile<D, QS>(sV, v + kvoff, j * 64, T);
@@ -236,7 +253,9 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int key = j * 64 + tx * 4 + c;
-        const float p = band_keep(row, key, T, wl, wr) ? exp2f(fmaf(s[i][c], sl2, -Lr[i])) : 0.f;
+        const float p = band_keep(row, key, T, wl, wr, lg_bits, lg_causal)
+                            ? exp2f(fmaf(s[i][c], sl2, -Lr[i]))
+                            : 0.f;
         ds[c] = p * (dp[i][c] - Dr[i]) * scale;
       }
       *reinterpret_cast<float4*>(sS + (ty * 8 + i) * PS + tx * 4) =
@@ -255,7 +274,8 @@ __global__ void __launch_bounds__(128)
                             const Tin* __restrict__ v, const Tin* __restrict__ d_o,
                             const float* __restrict__ delta, const float* __restrict__ lse2,
                             Tin* __restrict__ dk, Tin* __restrict__ dv, int B, int Hq, int Hkv,
-                            int T, int Tp, float scale, int wl, int wr) {
+                            int T, int Tp, float scale, int wl, int wr,
+                            const uint32_t* __restrict__ lg_bits, int lg_causal) {
   constexpr int QS = SimtCfg<D>::QS, PS = SimtCfg<D>::PS, OC = SimtCfg<D>::OC;
   extern __shared__ float4 smem4[];
   float* sK = reinterpret_cast<float*>(smem4);
@@ -285,8 +305,13 @@ __global__ void __launch_bounds__(128)
     for (int c = 0; c < OC; ++c) adk[i][c] = adv[i][c] = 0.f;
 
   // query blocks holding queries [k0 - wr, k0 + 63 + wl] (the transposed band)
-  const int i_lo = wr < 0 ? 0 : max(0, k0 - wr) / 64;
-  const int i_hi = wl < 0 ? n_t : min(n_t, min(T - 1, k0 + 63 + wl) / 64 + 1);
+  int i_lo = wr < 0 ? 0 : max(0, k0 - wr) / 64;
+  int i_hi = wl < 0 ? n_t : min(n_t, min(T - 1, k0 + 63 + wl) / 64 + 1);
+  if (lg_bits != nullptr && block_has_global(lg_bits, k0)) {
+    // a block with a global key is attended by every query (from the key on)
+    i_lo = lg_causal ? min(i_lo, k0 / 64) : 0;
+    i_hi = n_t;
+  }
   for (int g = 0; g < group; ++g) {
     const int bh = b * Hq + hk * group + g;
     const size_t qoff = static_cast<size_t>(bh) * T * D;
@@ -312,7 +337,9 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int qi = q0 + tx * 4 + c;
-          p[c] = band_keep(qi, key, T, wl, wr) ? exp2f(fmaf(s[i][c], sl2, -Lc[c])) : 0.f;
+          p[c] = band_keep(qi, key, T, wl, wr, lg_bits, lg_causal)
+                     ? exp2f(fmaf(s[i][c], sl2, -Lc[c]))
+                     : 0.f;
           ds[c] = p[c] * (dp[i][c] - Dc[c]) * scale;
         }
         *reinterpret_cast<float4*>(sP + (ty * 8 + i) * PS + tx * 4) =
@@ -345,13 +372,14 @@ fa_status launch_bwd_simt_impl(const BwdArgs& a) {
   using C = BwdSimtCfg<D>;
   auto kq = fa_bwd_dq_simt_kernel<Tin, D>;
   auto kkv = fa_bwd_dkdv_simt_kernel<Tin, D>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static bool attr_done[64] = {};  // per instantiation and device; benign race
+  bool* done = device_flag(attr_done);
+  if (done == nullptr || !*done) {
     cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DQ_SMEM);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DKDV_SMEM);
     if (e != cudaSuccess) return cuda_status(e);
-    attr_done = true;
+    if (done != nullptr) *done = true;
   }
   int wl, wr;
   effective_window(a, wl, wr);
@@ -362,13 +390,14 @@ fa_status launch_bwd_simt_impl(const BwdArgs& a) {
   kkv<<<static_cast<unsigned>(gkv), 128, C::DKDV_SMEM, a.stream>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
       static_cast<const Tin*>(a.d_o), a.ws_delta, a.ws_lse2, static_cast<Tin*>(a.dk),
-      static_cast<Tin*>(a.dv), a.B, a.Hq, a.Hkv, a.T, Tp, a.scale, wl, wr);
+      static_cast<Tin*>(a.dv), a.B, a.Hq, a.Hkv, a.T, Tp, a.scale, wl, wr,
+      a.local_global ? a.lg_bits : nullptr, a.causal);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
   kq<<<static_cast<unsigned>(gq), 128, C::DQ_SMEM, a.stream>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
       static_cast<const Tin*>(a.d_o), a.ws_delta, a.ws_lse2, static_cast<Tin*>(a.dq), a.B, a.Hq,
-      a.Hkv, a.T, Tp, a.scale, wl, wr);
+      a.Hkv, a.T, Tp, a.scale, wl, wr, a.local_global ? a.lg_bits : nullptr, a.causal);
   return cuda_status(cudaGetLastError());
 }
 

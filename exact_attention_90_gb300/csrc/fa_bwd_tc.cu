@@ -51,7 +51,7 @@ static __device__ unsigned int g_bwd_err;
 
 namespace {
 
-enum : int { kBwdMaskNone = 0, kBwdMaskCausal = 1, kBwdMaskBand = 2 };
+enum : int { kBwdMaskNone = 0, kBwdMaskCausal = 1, kBwdMaskBand = 2, kBwdMaskLocalGlobal = 3 };
 
 constexpr int kBwdThreads = 192;  // compute warps 0-3, producer 4, MMA 5
 
@@ -63,8 +63,9 @@ __device__ __forceinline__ int bwd_unit_index(int k) {
 // the band of the mask kind (a negative side: unbounded)
 template <int MASK>
 __device__ __forceinline__ void mask_window(int window_left, int window_right, int& wl, int& wr) {
-  wl = MASK == kBwdMaskBand ? window_left : -1;
-  wr = MASK == kBwdMaskBand ? window_right : (MASK == kBwdMaskCausal ? 0 : -1);
+  constexpr bool kBand = MASK == kBwdMaskBand || MASK == kBwdMaskLocalGlobal;
+  wl = kBand ? window_left : -1;
+  wr = kBand ? window_right : (MASK == kBwdMaskCausal ? 0 : -1);
 }
 
 // ============================================================ dK, dV kernel
@@ -90,6 +91,32 @@ __device__ __forceinline__ void kv_query_range(int kb, int T, int wl, int wr, in
   if (hi < lo) hi = lo;
 }
 
+// Local-global masks: a KV tile that holds a global key is attended by every
+// query (from the key on when causal), so its query steps run to the end.
+__device__ __forceinline__ void kv_query_range_lg(int kb, int T, int wl, int wr,
+                                                  const uint32_t* lg_bits, int causal, int& lo,
+                                                  int& hi) {
+  kv_query_range(kb, T, wl, wr, lo, hi);
+  const uint4 g = __ldg(reinterpret_cast<const uint4*>(lg_bits) + (kb >> 7));
+  const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+  int first = -1;  // first global key of the tile
+#pragma unroll
+  for (int i = 3; i >= 0; --i)
+    if (w[i] != 0u) first = kb + 32 * i + __ffs(static_cast<int>(w[i])) - 1;
+  if (first >= 0) {
+    lo = causal ? min(lo, first >> 6) : 0;
+    hi = (T + 63) >> 6;
+  }
+}
+
+// Bits e of a 32-column group starting at column `base` with lo <= base + e <= hi.
+__device__ __forceinline__ uint32_t range_bits32(int lo, int hi, int base) {
+  const int a = max(lo - base, 0), b = min(hi - base, 31);
+  if (a > b) return 0u;
+  const uint32_t upto_b = b >= 31 ? 0xffffffffu : ((1u << (b + 1)) - 1u);
+  return upto_b & ~((1u << a) - 1u);
+}
+
 template <int D, int MASK, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -99,7 +126,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           const float* __restrict__ delta, const float* __restrict__ lse2,
                           uint16_t* __restrict__ dK, uint16_t* __restrict__ dV, int B, int Hq,
                           int Hkv, int T, int Tp, float scale, float scale_log2, int num_units,
-                          int window_left, int window_right) {
+                          int window_left, int window_right, const uint32_t* __restrict__ lg_bits,
+                          int lg_causal) {
+  constexpr bool LG = MASK == kBwdMaskLocalGlobal;
   using C = KvCfg<D>;
   using TK = typename C::TK;
   using TQ = typename C::TQ;
@@ -186,7 +215,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         ++nu;
         int qlo, qhi;
-        kv_query_range(kb, T, wl, wr, qlo, qhi);
+        if constexpr (LG) kv_query_range_lg(kb, T, wl, wr, lg_bits, lg_causal, qlo, qhi);
+        else kv_query_range(kb, T, wl, wr, qlo, qhi);
         for (int g = 0; ok && g < group; ++g) {
           const int bh = b * Hq + hk * group + g;
           for (int qt = qlo; qt < qhi; ++qt) {
@@ -249,7 +279,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (idx >= num_units) break;
         const int j = idx / BHk;
         int qlo, qhi;
-        kv_query_range(j * 128, T, wl, wr, qlo, qhi);
+        if constexpr (LG) kv_query_range_lg(j * 128, T, wl, wr, lg_bits, lg_causal, qlo, qhi);
+        else kv_query_range(j * 128, T, wl, wr, qlo, qhi);
         const int nsteps = group * (qhi - qlo);
         if (!wait_bar(bar_kvfull, nu & 1, abort_flag, &g_bwd_err, kErrWaitMma)) break;
         ++nu;
@@ -300,7 +331,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int kb = j * 128;
       const int key = kb + r;
       int qlo, qhi;
-      kv_query_range(kb, T, wl, wr, qlo, qhi);
+      if constexpr (LG) kv_query_range_lg(kb, T, wl, wr, lg_bits, lg_causal, qlo, qhi);
+      else kv_query_range(kb, T, wl, wr, qlo, qhi);
+      // local-global: this key is a global key (kept for every query, from
+      // the key on when causal)
+      bool kglob = false;
+      if constexpr (LG) kglob = key < T && ((__ldg(lg_bits + (key >> 5)) >> (key & 31)) & 1u);
       const int nsteps = group * (qhi - qlo);
       for (int i = 0; i < nsteps; ++i, ++gs) {
         const int st = gs % NQS, bb = gs & 1;
@@ -327,8 +363,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float* dls = l2s + 64;
         // the tile needs the mask unless every (key, query) pair lies in the band
         const bool inside = (wr < 0 || kb + 127 <= q0 + wr) && (wl < 0 || kb >= q0 + 63 - wl);
-        const int c_lo = wr < 0 ? 0 : key - wr - q0;  // first kept query column
-        const int c_hi = wl < 0 ? 63 : key + wl - q0;  // last kept query column
+        int c_lo = wr < 0 ? 0 : key - wr - q0;  // first kept query column
+        int c_hi = wl < 0 ? 63 : key + wl - q0;  // last kept query column
+        if (LG && kglob) {
+          // a global key: the band widens to every query (from the key on)
+          c_lo = lg_causal ? key - q0 : 0;
+          c_hi = 63;
+        }
         uint32_t pp[32], dd[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -432,7 +473,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const float* __restrict__ delta, const float* __restrict__ lse2,
                         uint16_t* __restrict__ dQ, int B, int Hq, int Hkv, int T, int Tp,
                         float scale, float scale_log2, int num_units, int window_left,
-                        int window_right) {
+                        int window_right, const uint32_t* __restrict__ lg_bits,
+                        const int* __restrict__ lg_list, const int* __restrict__ lg_count,
+                        int lg_causal) {
+  constexpr bool LG = MASK == kBwdMaskLocalGlobal;
   using C = QCfg<D>;
   using TT = typename C::TT;
   constexpr int NSK = C::NSK, NSV = C::NSV;
@@ -498,8 +542,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int BH = B * Hq;
   const int n_qb = (T + 127) >> 7;
-  // unit idx: row block (last first: the longest when causal) and (b, h)
-  auto unit_of = [&](int idx, int& q0, int& bh, int& lo, int& hi) {
+  // unit idx: row block (last first: the longest when causal) and (b, h); its
+  // KV tiles are the band's [lo, hi) and, for local-global masks, the nb tiles
+  // holding a global key below lo plus those from list index ia up to the
+  // unit's last row (cnt tiles in all)
+  auto unit_of = [&](int idx, int& q0, int& bh, int& lo, int& hi, int& cnt, int& nb, int& ia) {
     q0 = (n_qb - 1 - idx / BH) * 128;
     bh = idx - (idx / BH) * BH;
     lo = wl < 0 ? 0 : max(0, q0 - wl) >> 7;
@@ -507,6 +554,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                   : min(static_cast<long long>(T) - 1,
                                         static_cast<long long>(q0) + 127 + wr);
     hi = static_cast<int>(last >> 7) + 1;
+    cnt = hi - lo;
+    nb = ia = 0;
+    if constexpr (LG) {
+      const int n = __ldg(lg_count);
+      const int cap = lg_causal ? min(T - 1, q0 + 127) >> 7 : (T - 1) >> 7;
+      auto lower_bound = [&](int x) {
+        int a = 0, b = n;
+        while (a < b) {
+          const int mid = (a + b) >> 1;
+          if (__ldg(lg_list + mid) < x) a = mid + 1;
+          else b = mid;
+        }
+        return a;
+      };
+      nb = lower_bound(lo);
+      ia = lower_bound(hi);
+      cnt += nb + max(0, lower_bound(cap + 1) - ia);
+    }
+  };
+  // KV tile of the unit's jj-th visited tile
+  auto tile_of = [&](int lo, int hi, int nb, int ia, int jj) -> int {
+    if constexpr (!LG) {
+      return lo + jj;
+    } else {
+      if (jj < nb) return __ldg(lg_list + jj);
+      if (jj < nb + (hi - lo)) return lo + (jj - nb);
+      return __ldg(lg_list + ia + (jj - nb - (hi - lo)));
+    }
   };
 
   if (warp == 4) {
@@ -523,8 +598,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int k = 0; ok; ++k) {
         const int idx = bwd_unit_index(k);
         if (idx >= num_units) break;
-        int q0, bh, lo, hi;
-        unit_of(idx, q0, bh, lo, hi);
+        int q0, bh, lo, hi, cnt, nb, ia;
+        unit_of(idx, q0, bh, lo, hi, cnt, nb, ia);
         const int b = bh / Hq, h = bh - b * Hq;
         const int zkv = b * Hkv + h / (Hq / Hkv);
         if (nu > 0 && !wait_bar(bar_qempty, (nu - 1) & 1, abort_flag, &g_bwd_err, kErrWaitLoad))
@@ -538,7 +613,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 pol_first);
         }
         ++nu;
-        for (int j = lo; j < hi; ++j) {
+        for (int jj = 0; jj < cnt; ++jj) {
+          const int j = tile_of(lo, hi, nb, ia, jj);
           const int sk = kc % NSK, sv = vc % NSV;
           if (kc >= NSK && !wait_bar(&bar_kempty[sk], ((kc / NSK) - 1) & 1, abort_flag,
                                      &g_bwd_err, kErrWaitLoad)) {
@@ -597,14 +673,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int k = 0; ok; ++k) {
         const int idx = bwd_unit_index(k);
         if (idx >= num_units) break;
-        int q0, bh, lo, hi;
-        unit_of(idx, q0, bh, lo, hi);
+        int q0, bh, lo, hi, cnt, nb, ia;
+        unit_of(idx, q0, bh, lo, hi, cnt, nb, ia);
         if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_bwd_err, kErrWaitMma)) break;
         ++nu;
         ptx::tc_fence_after();
         const int first = gs;
         const uint32_t q_lo = TT::kmajor_lo(aQ), do_lo = TT::kmajor_lo(adO);
-        for (int j = lo; j < hi; ++j) {
+        for (int jj = 0; jj < cnt; ++jj) {
           const int bb = gs & 1, sk = gs % NSK, sv = gs % NSV;
           if (!wait_bar(&bar_kfull[sk], (gs / NSK) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
             ok = false;
@@ -640,7 +716,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           ++gs;
         }
-        if (ok && hi > lo) ok = grad(gs - 1, first);
+        if (ok && cnt > 0) ok = grad(gs - 1, first);
         ptx::mma_commit(bar_qempty);
         ptx::mma_commit(bar_dq);
       }
@@ -657,13 +733,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int k = 0; ok; ++k) {
       const int idx = bwd_unit_index(k);
       if (idx >= num_units) break;
-      int q0, bh, lo, hi;
-      unit_of(idx, q0, bh, lo, hi);
+      int q0, bh, lo, hi, cnt, nb, ia;
+      unit_of(idx, q0, bh, lo, hi, cnt, nb, ia);
       const int q = q0 + r;
       const size_t wrow = static_cast<size_t>(bh) * Tp + q;  // q < Tp: rows are padded
       const float l2 = lse2[wrow];
       const float dl = delta[wrow];
-      for (int j = lo; j < hi; ++j, ++gs) {
+      for (int jj = 0; jj < cnt; ++jj, ++gs) {
+        const int j = tile_of(lo, hi, nb, ia, jj);
         const int bb = gs & 1;
         ok = __all_sync(0xffffffffu, wait_bar(&bar_sfull[bb], (gs >> 1) & 1, abort_flag,
                                               &g_bwd_err, kErrWaitSoftmax));
@@ -681,18 +758,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             (wl < 0 || kb >= q0 + 127 - wl);
         const int hi_c = (wr < 0 ? T - 1 : min(T - 1, q + wr)) - kb;  // last kept column
         const int lo_c = wl < 0 ? -1 : q - wl - kb;                     // first kept column
+        // local-global: the tile's global keys (before T, not after the row
+        // when causal) are kept as well
+        uint4 g4 = make_uint4(0u, 0u, 0u, 0u);
+        int ghi_c = -1;
+        if constexpr (LG) {
+          if (!inside) {
+            g4 = __ldg(reinterpret_cast<const uint4*>(lg_bits) + (kb >> 7));
+            ghi_c = (lg_causal ? min(T - 1, q) : T - 1) - kb;
+          }
+        }
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t s[32];
           ptx::tmem_ld32(tmem + lane_off + C::COL_S + bb * 128 + ch * 32, s);
           ptx::tmem_ld_wait(s);
+          uint32_t keep = 0xffffffffu;
+          if constexpr (LG) {
+            const uint32_t gw = ch == 0 ? g4.x : (ch == 1 ? g4.y : (ch == 2 ? g4.z : g4.w));
+            if (!inside)
+              keep = range_bits32(lo_c, hi_c, 32 * ch) | (gw & range_bits32(0, ghi_c, 32 * ch));
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = ch * 32 + e;
             float x0 = fmaf(__uint_as_float(s[e]), scale_log2, -l2);
             float x1 = fmaf(__uint_as_float(s[e + 1]), scale_log2, -l2);
-            if (!inside) {
+            if constexpr (LG) {
+              if (!((keep >> e) & 1u)) x0 = -INFINITY;
+              if (!((keep >> (e + 1)) & 1u)) x1 = -INFINITY;
+            } else if (!inside) {
               if (c > hi_c || c < lo_c) x0 = -INFINITY;
               if (c + 1 > hi_c || c + 1 < lo_c) x1 = -INFINITY;
             }
@@ -776,14 +872,15 @@ fa_status launch_bwd_tc_impl(const BwdArgs& a) {
   using CQ = QCfg<D>;
   auto kkv = fa_bwd_dkdv_tc_kernel<D, MASK, F16>;
   auto kq = fa_bwd_dq_tc_kernel<D, MASK, F16>;
-  static bool attr_done = false;  // per instantiation; benign race (idempotent)
-  if (!attr_done) {
+  static bool attr_done[64] = {};  // per instantiation and device; benign race
+  bool* done = device_flag(attr_done);
+  if (done == nullptr || !*done) {
     cudaError_t e =
         cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, CK::SMEM_BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e);
-    attr_done = true;
+    if (done != nullptr) *done = true;
   }
   using TK = TcTile<D, 128>;
   using TQ = TcTile<D, 64>;
@@ -817,12 +914,13 @@ fa_status launch_bwd_tc_impl(const BwdArgs& a) {
   kkv<<<static_cast<unsigned>(kv_units < sm ? kv_units : sm), kBwdThreads, CK::SMEM_BYTES,
         a.stream>>>(mq64, mdo64, mk, mv, a.ws_delta, a.ws_lse2, static_cast<uint16_t*>(a.dk),
                     static_cast<uint16_t*>(a.dv), a.B, a.Hq, a.Hkv, a.T, Tp, a.scale, scale_log2,
-                    static_cast<int>(kv_units), wl, wr);
+                    static_cast<int>(kv_units), wl, wr, a.lg_bits, a.causal);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
   kq<<<static_cast<unsigned>(q_units < sm ? q_units : sm), kBwdThreads, CQ::SMEM_BYTES,
        a.stream>>>(mq, mdo, mk, mv, a.ws_delta, a.ws_lse2, static_cast<uint16_t*>(a.dq), a.B,
-                   a.Hq, a.Hkv, a.T, Tp, a.scale, scale_log2, static_cast<int>(q_units), wl, wr);
+                   a.Hq, a.Hkv, a.T, Tp, a.scale, scale_log2, static_cast<int>(q_units), wl, wr,
+                   a.lg_bits, a.lg_list, a.lg_count, a.causal);
   return cuda_status(cudaGetLastError());
 }
 
@@ -841,6 +939,7 @@ template <bool F16>
 fa_status launch_bwd_tc_t(const BwdArgs& a) {
   int wl, wr;
   effective_window(a, wl, wr);
+  if (a.local_global) return launch_bwd_tc_d<kBwdMaskLocalGlobal, F16>(a);
   if (wl < 0 && wr < 0) return launch_bwd_tc_d<kBwdMaskNone, F16>(a);
   if (wl < 0 && wr == 0) return launch_bwd_tc_d<kBwdMaskCausal, F16>(a);
   return launch_bwd_tc_d<kBwdMaskBand, F16>(a);

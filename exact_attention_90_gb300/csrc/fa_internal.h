@@ -41,7 +41,15 @@ struct FwdArgs {
 size_t lg_workspace_bytes(int T);
 // Builds the bitmask and the tile list from `num_global` key indices (any
 // order; repeats and entries outside [0, T) select nothing more) into
-// `workspace` and points a.lg_* at them.
+// `workspace` (lg_workspace_bytes(T) bytes) on `stream`.
+struct LgSets {
+  const uint32_t* bits;
+  const int* list;
+  const int* count;
+};
+fa_status lg_prep(int T, const int* global_tokens, int num_global, void* workspace,
+                  cudaStream_t stream, LgSets* out);
+// The same for a forward call: points a.lg_* at the sets.
 fa_status launch_lg_prep(FwdArgs& a, const int* global_tokens, int num_global, void* workspace);
 
 // The band the kernels apply: the window intersected with causal (j <= i).
@@ -54,6 +62,16 @@ inline void band_of(int window_left, int window_right, int causal, int T, int& w
 }
 inline void effective_window(const FwdArgs& a, int& wl, int& wr) {
   band_of(a.window_left, a.window_right, a.causal, a.T, wl, wr);
+}
+
+// One-time setup per kernel and device (kernel attributes such as the dynamic
+// shared-memory limit are per device): the current device's slot in a
+// per-kernel table, or nullptr for a device index past the table (the caller
+// then repeats the setup on every call: correct, only slower).
+inline bool* device_flag(bool (&flags)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  return &flags[dev];
 }
 
 // Host-side argument checks shared by every entry point (no CUDA calls).
@@ -104,6 +122,12 @@ struct BwdArgs {
   float* ws_delta;  // [B*Hq][Tp] D_i = sum_c dO[i][c] O[i][c] (0 on padded rows)
   float* ws_lse2;   // [B*Hq][Tp] lse_i * log2(e) (+inf on padded rows)
   cudaStream_t stream;
+  // local-global mask (window_left = window_right = the local window), as in
+  // FwdArgs
+  bool local_global = false;
+  const uint32_t* lg_bits = nullptr;
+  const int* lg_list = nullptr;
+  const int* lg_count = nullptr;
 };
 
 // Query rows per head in the workspace: T rounded up to a multiple of 128.

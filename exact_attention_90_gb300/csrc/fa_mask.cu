@@ -66,26 +66,37 @@ size_t lg_workspace_bytes(int T) {
   return (tiles * 16 + tiles * 4 + 16 + 15) / 16 * 16;
 }
 
-fa_status launch_lg_prep(FwdArgs& a, const int* global_tokens, int num_global, void* workspace) {
-  const int n_tiles = (a.T + 127) / 128;
+fa_status lg_prep(int T, const int* global_tokens, int num_global, void* workspace,
+                  cudaStream_t stream, LgSets* out) {
+  const int n_tiles = (T + 127) / 128;
   uint32_t* bits = static_cast<uint32_t*>(workspace);
   int* list = reinterpret_cast<int*>(bits + static_cast<size_t>(n_tiles) * 4);
   int* count = list + n_tiles;
-  cudaError_t e = cudaMemsetAsync(bits, 0, static_cast<size_t>(n_tiles) * 16, a.stream);
+  cudaError_t e = cudaMemsetAsync(bits, 0, static_cast<size_t>(n_tiles) * 16, stream);
   if (e != cudaSuccess) return cuda_status(e);
   if (num_global > 0) {
     const int blocks = static_cast<int>(std::min<long long>((num_global + 255) / 256, 1024));
-    lg_scatter_kernel<<<blocks, 256, 0, a.stream>>>(global_tokens, num_global, bits, a.T);
+    lg_scatter_kernel<<<blocks, 256, 0, stream>>>(global_tokens, num_global, bits, T);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
-  lg_tiles_kernel<<<1, 1024, 0, a.stream>>>(bits, n_tiles, list, count);
+  lg_tiles_kernel<<<1, 1024, 0, stream>>>(bits, n_tiles, list, count);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
+  out->bits = bits;
+  out->list = list;
+  out->count = count;
+  return FA_OK;
+}
+
+fa_status launch_lg_prep(FwdArgs& a, const int* global_tokens, int num_global, void* workspace) {
+  LgSets g;
+  const fa_status s = lg_prep(a.T, global_tokens, num_global, workspace, a.stream, &g);
+  if (s != FA_OK) return s;
   a.local_global = true;
-  a.lg_bits = bits;
-  a.lg_list = list;
-  a.lg_count = count;
+  a.lg_bits = g.bits;
+  a.lg_list = g.list;
+  a.lg_count = g.count;
   return FA_OK;
 }
 

@@ -206,12 +206,13 @@ template <typename Tin, int D>
 fa_status launch_simt_impl(const FwdArgs& a) {
   using C = SimtCfg<D>;
   auto kern = fa_fwd_simt_kernel<Tin, D>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static bool attr_done[64] = {};  // per instantiation and device; benign race
+  bool* done = device_flag(attr_done);
+  if (done == nullptr || !*done) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e);
-    attr_done = true;
+    if (done != nullptr) *done = true;
   }
   const long long blocks = static_cast<long long>(a.B) * a.Hq * ((a.T + BQ - 1) / BQ);
   int wl, wr;

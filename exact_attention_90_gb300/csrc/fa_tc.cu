@@ -839,8 +839,9 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
   using C = TcCfg<D>;
   using Tile = TcTile<D>;
   auto kern = fa_fwd_tc_kernel<D, MASK, F16>;
-  static bool attr_done = false;  // per instantiation; benign race (idempotent)
-  if (!attr_done) {
+  static bool attr_done[64] = {};  // per instantiation and device; benign race
+  bool* done = device_flag(attr_done);
+  if (done == nullptr || !*done) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e);
@@ -850,7 +851,7 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
     e = cudaFuncGetAttributes(&fattr, kern);
     if (e != cudaSuccess) return cuda_status(e);
     if (C::REGS_SPLIT > C::THREADS * fattr.numRegs) return FA_ERR_UNSUPPORTED;
-    attr_done = true;
+    if (done != nullptr) *done = true;
   }
   CUtensorMap mq, mk, mv;
   CUresult r;

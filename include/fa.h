@@ -216,6 +216,24 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * sizes. */
 unsigned long long fa_bwd_workspace_size(int B, int Hq, int T);
 
+/* Backward of the local-global forward (fa_fwd_local_global): the same
+ * gradients as fa_bwd for the mask |i - j| <= local_window OR j in
+ * global_tokens (intersected with j <= i when causal).  o and lse must come
+ * from fa_fwd_local_global with the same mask.  Arguments as fa_bwd, with the
+ * mask arguments of fa_fwd_local_global; the workspace is at least
+ * fa_bwd_local_global_workspace_size(B, Hq, T) bytes (fa_bwd's rows plus the
+ * key sets).  Errors: as fa_bwd and fa_fwd_local_global. */
+fa_status fa_bwd_local_global(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                              int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                              int local_window, const int* global_tokens, int num_global,
+                              fa_dtype dtype, void* workspace,
+                              unsigned long long workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_bwd_local_global needs: fa_bwd_workspace_size(B, Hq,
+ * T) + fa_fwd_local_global_workspace_size(T); 0 for invalid sizes. */
+unsigned long long fa_bwd_local_global_workspace_size(int B, int Hq, int T);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -39,7 +39,7 @@ from .attention_ref import _check_shapes, as_f64, kv_head_of, valid_keys
 
 
 def attention_bwd_head_ref(qh, kh, vh, doh, scale: float, causal: bool, window=None,
-                           row_chunk: int = 256):
+                           row_chunk: int = 256, global_tokens=None):
     """The chain-rule gradients for one query head (2-D [T, d] fp64 arrays).
 
     Returns (dQ_h [T, d], dK_h [T, d], dV_h [T, d]): dQ of this query head and
@@ -55,7 +55,7 @@ def attention_bwd_head_ref(qh, kh, vh, doh, scale: float, causal: bool, window=N
     for r0 in range(0, T, row_chunk):
         rows = np.arange(r0, min(T, r0 + row_chunk))
         s = (qh[rows] @ kh.T) * scale
-        valid = valid_keys(rows, T, causal, window)
+        valid = valid_keys(rows, T, causal, window, global_tokens)
         s = np.where(valid, s, -np.inf)
         m = s.max(axis=1)
         e = np.where(valid, np.exp(s - m[:, None]), 0.0)
@@ -69,13 +69,13 @@ def attention_bwd_head_ref(qh, kh, vh, doh, scale: float, causal: bool, window=N
 
 
 def attention_bwd_ref(q, k, v, do, scale: float, causal: bool, window=None,
-                      row_chunk: int = 256):
+                      row_chunk: int = 256, global_tokens=None):
     """Gradients of the attention forward with respect to Q, K and V (fp64).
 
     Args:
       q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; do: [B, Hq, T, d], the
         upstream gradient of O (any real dtype, numpy or torch).
-      scale, causal, window: as for ``attention_ref``.
+      scale, causal, window, global_tokens: as for ``attention_ref``.
 
     Returns:
       (dQ [B, Hq, T, d], dK [B, Hkv, T, d], dV [B, Hkv, T, d]) in fp64.
@@ -91,7 +91,7 @@ def attention_bwd_ref(q, k, v, do, scale: float, causal: bool, window=None,
         for h in range(Hq):
             hk = kv_head_of(h, Hq, Hkv)
             dq, dk, dv = attention_bwd_head_ref(q[b, h], k[b, hk], v[b, hk], do[b, h], scale,
-                                                causal, window, row_chunk)
+                                                causal, window, row_chunk, global_tokens)
             dQ[b, h] = dq
             dK[b, hk] += dk
             dV[b, hk] += dv

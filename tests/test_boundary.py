@@ -287,3 +287,27 @@ def test_local_global_rejects_bad_arguments_on_the_host(lib):
     assert lg_call(gt=O + 64) == fa.FA_ERR_INVALID_ARG       # tokens overlap an output
     assert lg_call(q=0) == fa.FA_ERR_INVALID_ARG             # the fa_fwd checks apply
     assert lg_call(d=40) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_bwd_local_global_workspace_and_host_errors(lib):
+    assert (fa.fa_bwd_local_global_workspace_size(2, 4, 100)
+            == fa.fa_bwd_workspace_size(2, 4, 100) + fa.fa_fwd_local_global_workspace_size(100))
+    assert fa.fa_bwd_local_global_workspace_size(0, 4, 100) == 0
+    need = fa.fa_bwd_local_global_workspace_size(GOOD["B"], GOOD["Hq"], GOOD["T"])
+
+    def call(w=3, gt=GT, n=5, ws=BWS, ws_bytes=need, **kw):
+        a = dict(GOOD, d_o=DO, dq=DQ, dk=DK, dv=DV)
+        a.update(kw)
+        return fa.fa_bwd_local_global(a["q"], a["k"], a["v"], a["o"], a["lse"], a["d_o"], a["dq"],
+                                      a["dk"], a["dv"], a["B"], a["Hq"], a["Hkv"], a["T"], a["d"],
+                                      a["scale"], a["causal"], w, gt, n, a["dtype"], ws, ws_bytes,
+                                      stream=0)
+
+    assert call(w=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(n=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(gt=0, n=2) == fa.FA_ERR_INVALID_ARG
+    assert call(gt=GT + 2) == fa.FA_ERR_MISALIGNED
+    assert call(ws_bytes=need - 16) == fa.FA_ERR_WORKSPACE      # the key sets do not fit
+    assert call(dq=GT) == fa.FA_ERR_INVALID_ARG                  # dQ overlaps the token list
+    assert call(dq=0) == fa.FA_ERR_INVALID_ARG                   # the fa_bwd checks apply
+    assert call(d=24) == fa.FA_ERR_UNSUPPORTED

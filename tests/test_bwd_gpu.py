@@ -181,3 +181,29 @@ def test_bwd_full_size_sampled_heads(cuda_lib, B, H, T, d, causal):
     for b, h in ((0, 0), (B - 1, H - 1)):
         ref = oracle.attention_bwd_head_ref(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
         check_grads((dq[b, h], dk[b, h], dv[b, h]), ref, "bf16", f"head ({b},{h}) T={T}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T,d,w,tokens", [(129, 32, 0, [0]), (640, 128, 5, [0, 1, 2, 3]),
+                                          (1000, 64, 64, [999, 17, 17, -4, 1500, 300]),
+                                          (777, 16, 2, []), (2500, 128, 100, "strided")])
+def test_bwd_local_global(cuda_lib, T, d, w, tokens, causal, dtype):
+    """Backward of the local-global mask: key tiles holding a global key are
+    visited by every query step (dK, dV) and by every row tile (dQ)."""
+    fa = cuda_lib
+    g = list(range(7, T, 113)) if tokens == "strided" else tokens
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_qkv(1, 2, 1, T, d, dtype=dtype, seed=T + w)
+    do = make_grad_out(1, 2, T, d, dtype=dtype, seed=T + w)
+    qc, kc, vc, doc = (x.cuda() for x in (q, k, v, do))
+    gt = torch.tensor(g, dtype=torch.int32, device="cuda")
+    O, L = oracle.attention_ref(q, k, v, scale, causal, window=(w, w), global_tokens=g)
+    o = torch.from_numpy(O).to(DTYPES[dtype]).cuda()
+    lse = torch.from_numpy(L).to(torch.float32).cuda()
+    grads = fa.bwd(qc, kc, vc, o, lse, doc, causal=causal, scale=scale, window=(w, w),
+                   global_tokens=gt)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+    ref = oracle.attention_bwd_ref(q, k, v, do, scale, causal, window=(w, w), global_tokens=g)
+    check_grads(grads, ref, dtype, f"local-global T={T} d={d} w={w} causal={causal} {dtype}")

@@ -133,6 +133,31 @@ def pin_bwd_library_autograd(bwd):
         np.testing.assert_allclose(dV, vt.grad.numpy(), rtol=0, atol=1e-12)
 
 
+def pin_bwd_local_global_autograd(bwd):
+    """Local-global masks (band OR global key, then causal) against torch
+    autograd through SDPA with the tutorial's mask written out."""
+    for n, (T, w, g, causal) in enumerate(((30, 2, [0, 1], True), (27, 0, [26, 5, 5, -1], False),
+                                           (33, 3, [], True))):
+        q, k, v, do = _rand(1, 2, 1, T, 8, seed=60 + n)
+        scale = 0.45
+        dQ, dK, dV = bwd(q, k, v, do, scale, causal, window=(w, w), global_tokens=g)
+        qt = torch.tensor(q, requires_grad=True)
+        kt = torch.tensor(k, requires_grad=True)
+        vt = torch.tensor(v, requires_grad=True)
+        i = torch.arange(T)[:, None]
+        j = torch.arange(T)[None, :]
+        mask = ((i - j).abs() <= w) | torch.isin(j, torch.tensor(g, dtype=torch.long))
+        if causal:
+            mask &= j <= i
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt.repeat_interleave(2, dim=1), vt.repeat_interleave(2, dim=1), attn_mask=mask,
+            scale=scale)
+        o.backward(torch.tensor(do))
+        np.testing.assert_allclose(dQ, qt.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dK, kt.grad.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dV, vt.grad.numpy(), rtol=0, atol=1e-12)
+
+
 def pin_bwd_invariants(bwd):
     """Key gradients sum to 0 over the keys; value gradients sum to the
     group's summed dO; shifting all keys by one vector changes no gradient;
@@ -169,7 +194,7 @@ def pin_bwd_closed_forms(bwd):
 
 
 PINS = [pin_bwd_directional_fd, pin_bwd_elementwise_fd_brute, pin_bwd_library_autograd,
-        pin_bwd_invariants, pin_bwd_closed_forms]
+        pin_bwd_local_global_autograd, pin_bwd_invariants, pin_bwd_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -199,11 +224,11 @@ def _mutant_head(mistake):
     """A copy of the per-head chain-rule step with one planted mistake."""
     from oracle.attention_ref import valid_keys
 
-    def head(qh, kh, vh, doh, scale, causal, window=None):
+    def head(qh, kh, vh, doh, scale, causal, window=None, global_tokens=None):
         T, d = qh.shape
         rows = np.arange(T)
         s = (qh @ kh.T) * scale
-        valid = valid_keys(rows, T, causal, window)
+        valid = valid_keys(rows, T, causal, window, global_tokens)
         if mistake == "mask_dropped":
             valid = np.ones_like(valid)
         s = np.where(valid, s, -np.inf)
@@ -223,7 +248,7 @@ def _mutant_head(mistake):
         dk = scale * ((ds @ qh) if mistake == "dk_untransposed" else (ds.T @ qh))
         return dq, dk, dv
 
-    def bwd(q, k, v, do, scale, causal, window=None):
+    def bwd(q, k, v, do, scale, causal, window=None, global_tokens=None):
         q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
         B, Hq, T, d = q.shape
         Hkv = k.shape[1]
@@ -233,7 +258,8 @@ def _mutant_head(mistake):
         for b in range(B):
             for h in range(Hq):
                 hk = h // (Hq // Hkv) if mistake != "head_modulo" else h % Hkv
-                dq, dk, dv = head(q[b, h], k[b, hk], v[b, hk], do[b, h], scale, causal, window)
+                dq, dk, dv = head(q[b, h], k[b, hk], v[b, hk], do[b, h], scale, causal, window,
+                                  global_tokens)
                 dQ[b, h] = dq
                 if mistake == "no_group_sum":
                     dK[b, hk] = dk
