@@ -25,7 +25,8 @@ Contents (each function cites the passage it follows):
 * ``attention_bwd_ref``  -- the gradients of the forward with respect to Q, K
                             and V for an upstream gradient dO, by the chain
                             rule in fp64 (the backward oracle);
-                            ``attention_bwd_head_ref`` is its one-head step.
+                            ``attention_bwd_head_ref`` is its one-head step,
+                            ``attention_bwd_dq_rows_ref`` dQ for chosen rows.
 * ``naive_score_bytes``  -- bytes of the T x T score matrix that the naive path
                             materialises (the pages' memory table).
 
@@ -44,7 +45,7 @@ from .attention_ref import (
     naive_score_bytes,
     valid_keys,
 )
-from .attention_bwd_ref import attention_bwd_head_ref, attention_bwd_ref
+from .attention_bwd_ref import attention_bwd_dq_rows_ref, attention_bwd_head_ref, attention_bwd_ref
 from .brute import attention_brute
 from .online_ref import attention_online_ref
 
@@ -57,6 +58,7 @@ __all__ = [
     "attention_brute",
     "attention_bwd_ref",
     "attention_bwd_head_ref",
+    "attention_bwd_dq_rows_ref",
     "kv_head_of",
     "naive_score_bytes",
     "valid_keys",

@@ -96,3 +96,26 @@ def attention_bwd_ref(q, k, v, do, scale: float, causal: bool, window=None,
             dK[b, hk] += dk
             dV[b, hk] += dv
     return dQ, dK, dV
+
+
+def attention_bwd_dq_rows_ref(q, k, v, do, scale: float, causal: bool, b: int, h: int, rows,
+                              window=None, global_tokens=None):
+    """dQ for selected query rows of one (b, h) only (fp64).
+
+    Exact for those rows: dQ_i = scale * sum_j dS_ij k_j needs only row i of
+    P and dP (and so only row i of Q and dO), which makes full-size checks
+    of dQ affordable.  Returns dQ_rows [len(rows), d].
+    """
+    q, k, v, do = as_f64(q), as_f64(k), as_f64(v), as_f64(do)
+    B, Hq, Hkv, T, d = _check_shapes(q, k, v)
+    rows = np.asarray(rows, dtype=np.int64)
+    hk = kv_head_of(h, Hq, Hkv)
+    kh, vh = k[b, hk], v[b, hk]
+    s = (q[b, h][rows] @ kh.T) * scale
+    valid = valid_keys(rows, T, causal, window, global_tokens)
+    s = np.where(valid, s, -np.inf)
+    e = np.where(valid, np.exp(s - s.max(axis=1)[:, None]), 0.0)
+    p = e / e.sum(axis=1)[:, None]
+    dp = do[b, h][rows] @ vh.T
+    ds = p * (dp - (p * dp).sum(axis=1)[:, None])
+    return scale * (ds @ kh)

@@ -294,3 +294,15 @@ def test_bwd_planted_mistake_is_caught(mistake):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"planted mistake {mistake!r} passed every pin"
+
+
+def test_bwd_dq_rows_equal_the_full_backward():
+    """The rows-only dQ is the full backward's dQ for those rows (every mask)."""
+    q, k, v, do = _rand(2, 4, 2, 37, 8, seed=17)
+    for causal, window, g in ((False, None, None), (True, None, None), (False, (3, 5), None),
+                              (True, (2, 2), [0, 30])):
+        dQ, _, _ = oracle.attention_bwd_ref(q, k, v, do, 0.3, causal, window=window, global_tokens=g)
+        rows = [0, 5, 36, 17]
+        got = oracle.attention_bwd_dq_rows_ref(q, k, v, do, 0.3, causal, 1, 3, rows, window=window,
+                                               global_tokens=g)
+        np.testing.assert_allclose(got, dQ[1, 3, rows], rtol=0, atol=1e-13)
