@@ -29,7 +29,7 @@ __all__ = [
     "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
     "fa_fwd_local_global", "fa_fwd_local_global_workspace_size", "fa_bwd_local_global",
-    "fa_bwd_local_global_workspace_size",
+    "fa_bwd_local_global_workspace_size", "fa_fwd_host", "fa_fwd_host_workspace_size", "fwd_host",
     "bwd", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
@@ -76,6 +76,9 @@ EXPORTS = [
     ("fa_bwd_local_global", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
                                  _I, _P, _I, _I, _P, ctypes.c_ulonglong, _P]),
     ("fa_bwd_local_global_workspace_size", ctypes.c_ulonglong, [_I, _I, _I]),
+    ("fa_fwd_host", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
+                         ctypes.c_ulonglong, _P]),
+    ("fa_fwd_host_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I, _I, _I]),
 ]
 
 
@@ -235,6 +238,20 @@ def fa_bwd_local_global(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scal
 
 def fa_bwd_local_global_workspace_size(B, Hq, T) -> int:
     return load_library().fa_bwd_local_global_workspace_size(int(B), int(Hq), int(T))
+
+
+def fa_fwd_host(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, chunks, workspace,
+                workspace_bytes, stream=None) -> int:
+    """The C function fa_fwd_host (host buffers in and out, chunks pipelined)."""
+    lib = load_library()
+    return lib.fa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                           int(Hkv), int(T), int(d), float(scale), int(causal), int(dtype),
+                           int(chunks), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_host_workspace_size(B, Hq, Hkv, T, d, dtype, chunks) -> int:
+    return load_library().fa_fwd_host_workspace_size(int(B), int(Hq), int(Hkv), int(T), int(d),
+                                                     int(dtype), int(chunks))
 
 
 def fa_bwd_workspace_size(B, Hq, T) -> int:
@@ -428,3 +445,42 @@ def bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None, 
                 wr, code, ws, nbytes, stream)
     _check(st, "fa_bwd")
     return dq, dk, dv
+
+
+def fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             chunks: int = 4, workspace=None, stream=None, device=None):
+    """Attention forward on host (CPU) tensors, copies overlapped with compute.
+
+    q, k, v: contiguous CPU tensors [B, H, T, d] (pinned memory gives the
+    overlap); out and lse are CPU tensors (allocated pinned when omitted).
+    The batch runs in ``chunks`` pipelined chunks; the device workspace is
+    allocated with torch on ``device`` (default: the current CUDA device)
+    unless given.  Asynchronous on ``stream``: synchronise it before reading
+    the outputs.  Returns (out, lse).
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise TypeError(f"{name} must be a CPU tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor [B, H, T, d]")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32).pin_memory()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    nbytes = fa_fwd_host_workspace_size(B, Hq, Hkv, T, d, code, chunks)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = fa_fwd_host(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), code, chunks,
+                     workspace, nbytes, stream)
+    _check(st, "fa_fwd_host")
+    return out, lse

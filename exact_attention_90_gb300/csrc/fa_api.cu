@@ -315,6 +315,30 @@ unsigned long long fa_bwd_local_global_workspace_size(int B, int Hq, int T) {
   return fa::bwd_workspace_bytes(B, Hq, T) + fa::lg_workspace_bytes(T);
 }
 
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int T, int d, float scale, int causal, fa_dtype dtype,
+                      int chunks, void* workspace, unsigned long long workspace_bytes,
+                      void* stream) {
+  fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype,
+                static_cast<cudaStream_t>(stream)};
+  fa_status s = fa::validate_fwd(a);
+  if (s != FA_OK) return s;
+  if (chunks < 1) return FA_ERR_INVALID_ARG;
+  if (chunks > B) chunks = B;
+  if (workspace == nullptr) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
+  if (workspace_bytes < fa::host_workspace_bytes(B, Hq, Hkv, T, d, dtype, chunks))
+    return FA_ERR_WORKSPACE;
+  return fa::run_fwd_host(a, chunks, workspace);
+}
+
+unsigned long long fa_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d,
+                                              fa_dtype dtype, int chunks) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || d <= 0 || chunks < 1) return 0;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 0;
+  return fa::host_workspace_bytes(B, Hq, Hkv, T, d, dtype, chunks > B ? B : chunks);
+}
+
 unsigned long long fa_bwd_workspace_size(int B, int Hq, int T) {
   if (B <= 0 || Hq <= 0 || T <= 0) return 0;
   return fa::bwd_workspace_bytes(B, Hq, T);

@@ -147,6 +147,13 @@ fa_status launch_bwd_tc(const BwdArgs& a);
 bool bwd_tc_supported(const BwdArgs& a);
 fa_status bwd_read_and_clear_error(unsigned int* word);
 
+// ------------------------------------------------------------- host buffers
+// Device workspace of fa_fwd_host: two chunk slots of Q, K, V, O and LSE.
+size_t host_workspace_bytes(int B, int Hq, int Hkv, int T, int d, fa_dtype dtype, int chunks);
+// Forward from host q, k, v to host o, lse (a.* hold host pointers), in
+// `chunks` batch chunks pipelined over two internal streams.
+fa_status run_fwd_host(const FwdArgs& a, int chunks, void* workspace);
+
 // Device error word shared by the kernels (read-and-clear, synchronous).
 fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
 

@@ -234,6 +234,33 @@ fa_status fa_bwd_local_global(const void* q, const void* k, const void* v, const
  * T) + fa_fwd_local_global_workspace_size(T); 0 for invalid sizes. */
 unsigned long long fa_bwd_local_global_workspace_size(int B, int Hq, int T);
 
+/* Forward from HOST buffers to HOST buffers.  Same operation, sizes and
+ * layouts as fa_fwd, but q, k, v, o and lse are host pointers (pinned memory,
+ * e.g. cudaHostAlloc, lets the copies run asynchronously and overlap; pageable
+ * memory works, without overlap).  The batch is cut into `chunks` chunks of
+ * whole batch entries; each chunk's inputs are copied to the device, its
+ * attention computed and its outputs copied back, with the chunks alternating
+ * between two streams of the library (created once per device) so that copies
+ * overlap kernels.  The work is ordered after everything already on `stream`
+ * and everything later on `stream` is ordered after it; the call returns
+ * without synchronising (the host outputs are complete once `stream` has
+ * reached this point).  Calls on one device run on the GPU in turn.
+ *   chunks    : 1 .. B (larger values are clamped to B); each chunk should
+ *               keep the GPU busy (B*Hq*ceil(T/256)/chunks work units of 256
+ *               rows against the number of SMs)
+ *   workspace : DEVICE scratch of at least fa_fwd_host_workspace_size(...)
+ *               bytes (two chunks of q, k, v, o and lse), 16-byte aligned
+ * Errors: as fa_fwd (for the host pointers), plus FA_ERR_INVALID_ARG for
+ * chunks < 1 and FA_ERR_WORKSPACE for a NULL or too small workspace. */
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int Hq, int Hkv, int T, int d, float scale, int causal,
+                      fa_dtype dtype, int chunks, void* workspace,
+                      unsigned long long workspace_bytes, void* stream);
+
+/* Bytes of device workspace fa_fwd_host needs; 0 for invalid arguments. */
+unsigned long long fa_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d,
+                                              fa_dtype dtype, int chunks);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 
