@@ -11,10 +11,10 @@ line (rank 0):
 
   value      TFLOP/s, flops = 4*B*Hq*T^2*d halved when causal, inputs resident
              in HBM, CUDA events on the launching stream, max over ranks
-  e2e        the same metric with pinned-host inputs copied in and O, LSE
-             copied out inside every timed step, through the C ABI's
-             host-buffer entry point fa_fwd_host (batch chunks pipelined so
-             that the copies overlap the kernels)
+  e2e        the same metric with pinned-host inputs copied in and the
+             outputs copied out inside every timed step, through the C ABI's
+             host-buffer entry points fa_fwd_host / fa_bwd_host (batch chunks
+             pipelined so that the copies overlap the kernels)
   roofline   the kernel against the measured bf16 dense peak (burst figure:
              each launch is timed as a kernel of its own)
   cpu_baseline  the fp64 CPU oracle, as it stands, on a bounded sample of the
@@ -392,17 +392,18 @@ def run_ours(args, w):
     # forward: the C ABI's host-buffer entry point, which pipelines batch
     # chunks so that copies overlap the kernels (about 256 work units per chunk)
     chunks = max(1, min(w.B, w.B * w.Hq * ((w.T + 255) // 256) // 256))
-    if not bwd:
-        hws_bytes = fa.fa_fwd_host_workspace_size(w.B, w.Hq, w.Hkv, w.T, w.d, code, chunks)
-        hws = torch.empty(hws_bytes, dtype=torch.uint8, device=dev)
+    size_fn = fa.fa_bwd_host_workspace_size if bwd else fa.fa_fwd_host_workspace_size
+    hws_bytes = size_fn(w.B, w.Hq, w.Hkv, w.T, w.d, code, chunks)
+    hws = torch.empty(hws_bytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
         if bwd:
-            for dst, src in ins:
-                dst.copy_(src, non_blocking=True)
-            fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv)
-            for src, dst in outs:
-                dst.copy_(src, non_blocking=True)
+            h = [src for _, src in ins]  # q, k, v, o, lse, dO (pinned)
+            st = fa.fa_bwd_host(h[0], h[1], h[2], h[3], h[4], h[5], outs[0][1], outs[1][1],
+                                outs[2][1], w.B, w.Hq, w.Hkv, w.T, w.d, w.scale, int(w.causal),
+                                -1, -1, code, chunks, hws, hws_bytes, stream)
+            if st != 0:
+                raise fa.FaError(st, "fa_bwd_host")
         else:
             st = fa.fa_fwd_host(qp, kp, vp, outs[0][1], outs[1][1], w.B, w.Hq, w.Hkv, w.T, w.d,
                                 w.scale, int(w.causal), code, chunks, hws, hws_bytes, stream)
@@ -442,9 +443,8 @@ def run_ours(args, w):
         "config": config_of(w, world),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": ("torch copies on the stream around fa_bwd" if bwd else
-                         f"fa_fwd_host: pinned host buffers, {chunks} batch chunks "
-                         "pipelined over 2 streams")},
+                "path": (f"{'fa_bwd_host' if bwd else 'fa_fwd_host'}: pinned host buffers, "
+                         f"{chunks} batch chunks pipelined over 2 streams")},
         "gpu_launches": args.steps * (3 if bwd else 1),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": (achieved / peak) if peak else None, "traffic": traffic,

@@ -30,6 +30,7 @@ __all__ = [
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
     "fa_fwd_local_global", "fa_fwd_local_global_workspace_size", "fa_bwd_local_global",
     "fa_bwd_local_global_workspace_size", "fa_fwd_host", "fa_fwd_host_workspace_size", "fwd_host",
+    "fa_bwd_host", "fa_bwd_host_workspace_size", "bwd_host",
     "bwd", "FA_DTYPE_F32",
     "FA_DTYPE_BF16", "FA_DTYPE_F16",
 ]
@@ -79,6 +80,9 @@ EXPORTS = [
     ("fa_fwd_host", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
                          ctypes.c_ulonglong, _P]),
     ("fa_fwd_host_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I, _I, _I]),
+    ("fa_bwd_host", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I,
+                         _I, _I, _P, ctypes.c_ulonglong, _P]),
+    ("fa_bwd_host_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I, _I, _I]),
 ]
 
 
@@ -251,6 +255,22 @@ def fa_fwd_host(q, k, v, o, lse, B, Hq, Hkv, T, d, scale, causal, dtype, chunks,
 
 def fa_fwd_host_workspace_size(B, Hq, Hkv, T, d, dtype, chunks) -> int:
     return load_library().fa_fwd_host_workspace_size(int(B), int(Hq), int(Hkv), int(T), int(d),
+                                                     int(dtype), int(chunks))
+
+
+def fa_bwd_host(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal, window_left,
+                window_right, dtype, chunks, workspace, workspace_bytes, stream=None) -> int:
+    """The C function fa_bwd_host (host buffers in and out, chunks pipelined)."""
+    lib = load_library()
+    return lib.fa_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq),
+                           _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(T), int(d),
+                           float(scale), int(causal), int(window_left), int(window_right),
+                           int(dtype), int(chunks), _ptr(workspace), int(workspace_bytes),
+                           _stream(stream))
+
+
+def fa_bwd_host_workspace_size(B, Hq, Hkv, T, d, dtype, chunks) -> int:
+    return load_library().fa_bwd_host_workspace_size(int(B), int(Hq), int(Hkv), int(T), int(d),
                                                      int(dtype), int(chunks))
 
 
@@ -484,3 +504,36 @@ def fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None
                      workspace, nbytes, stream)
     _check(st, "fa_fwd_host")
     return out, lse
+
+
+def bwd_host(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None,
+             window=None, chunks: int = 4, dq=None, dk=None, dv=None, workspace=None,
+             stream=None, device=None):
+    """Attention backward on host (CPU) tensors, copies overlapped with compute.
+
+    Arguments as ``bwd`` with CPU tensors (pinned memory gives the overlap);
+    dq, dk, dv are allocated pinned when omitted.  Asynchronous on ``stream``:
+    synchronise it before reading the gradients.  Returns (dq, dk, dv).
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("d_o", d_o), ("lse", lse)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CPU tensor")
+    B, Hq, T, d = q.shape
+    Hkv = k.shape[1]
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty(q.shape, dtype=q.dtype).pin_memory() if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype).pin_memory() if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype).pin_memory() if dv is None else dv
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    nbytes = fa_bwd_host_workspace_size(B, Hq, Hkv, T, d, code, chunks)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = fa_bwd_host(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, int(bool(causal)),
+                     wl, wr, code, chunks, workspace, nbytes, stream)
+    _check(st, "fa_bwd_host")
+    return dq, dk, dv

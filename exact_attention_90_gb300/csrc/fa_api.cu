@@ -332,6 +332,48 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
   return fa::run_fwd_host(a, chunks, workspace);
 }
 
+fa_status fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                      int T, int d, float scale, int causal, int window_left, int window_right,
+                      fa_dtype dtype, int chunks, void* workspace,
+                      unsigned long long workspace_bytes, void* stream) {
+  fa::FwdArgs f{q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, Hq, Hkv, T, d, scale,
+                causal, dtype, static_cast<cudaStream_t>(stream)};
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  fa_status s = fa::validate_fwd(f);
+  if (s != FA_OK) return s;
+  if (!d_o || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned16(d_o) || !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  if (chunks < 1) return FA_ERR_INVALID_ARG;
+  if (chunks > B) chunks = B;
+  if (workspace == nullptr) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
+  if (workspace_bytes < fa::bwd_host_workspace_bytes(B, Hq, Hkv, T, d, dtype, chunks))
+    return FA_ERR_WORKSPACE;
+  const size_t e = dtype == FA_DTYPE_F32 ? 4 : 2;
+  const size_t nq = static_cast<size_t>(B) * Hq * T * d * e;
+  const size_t nkv = static_cast<size_t>(B) * Hkv * T * d * e;
+  const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
+  // the host gradients against every host buffer
+  const void* bufs[9] = {q, k, v, o, lse, d_o, dq, dk, dv};
+  const size_t lens[9] = {nq, nkv, nkv, nq, nl, nq, nq, nkv, nkv};
+  for (int w = 6; w < 9; ++w)
+    for (int x = 0; x < 9; ++x)
+      if (x != w && fa::overlap(bufs[w], lens[w], bufs[x], lens[x])) return FA_ERR_INVALID_ARG;
+  fa::BwdArgs a{q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
+                window_left, window_right, dtype, nullptr, nullptr,
+                static_cast<cudaStream_t>(stream)};
+  return fa::run_bwd_host(a, chunks, workspace);
+}
+
+unsigned long long fa_bwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d,
+                                              fa_dtype dtype, int chunks) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || d <= 0 || chunks < 1) return 0;
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 0;
+  return fa::bwd_host_workspace_bytes(B, Hq, Hkv, T, d, dtype, chunks > B ? B : chunks);
+}
+
 unsigned long long fa_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d,
                                               fa_dtype dtype, int chunks) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || d <= 0 || chunks < 1) return 0;

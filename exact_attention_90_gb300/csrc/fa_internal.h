@@ -153,6 +153,11 @@ size_t host_workspace_bytes(int B, int Hq, int Hkv, int T, int d, fa_dtype dtype
 // Forward from host q, k, v to host o, lse (a.* hold host pointers), in
 // `chunks` batch chunks pipelined over two internal streams.
 fa_status run_fwd_host(const FwdArgs& a, int chunks, void* workspace);
+// Device workspace of fa_bwd_host, and the backward from host buffers (a.*
+// hold host pointers; a.ws_* are unused: each chunk slot holds its own rows)
+size_t bwd_host_workspace_bytes(int B, int Hq, int Hkv, int T, int d, fa_dtype dtype,
+                                int chunks);
+fa_status run_bwd_host(const BwdArgs& a, int chunks, void* workspace);
 
 // Device error word shared by the kernels (read-and-clear, synchronous).
 fa_status read_and_clear_device_error(cudaStream_t stream, unsigned int* word);

@@ -261,6 +261,24 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
 unsigned long long fa_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d,
                                               fa_dtype dtype, int chunks);
 
+/* Backward from HOST buffers to HOST buffers: fa_bwd's operation, sizes and
+ * mask arguments with q, k, v, o, lse, d_o, dq, dk and dv on the host, in
+ * `chunks` batch chunks pipelined over the library's two streams exactly as
+ * fa_fwd_host does (same ordering, asynchrony and pinning notes).
+ *   workspace : DEVICE scratch of at least fa_bwd_host_workspace_size(...)
+ *               bytes (two chunk slots of every tensor and the rows' part)
+ * Errors: as fa_bwd (for the host pointers), plus FA_ERR_INVALID_ARG for
+ * chunks < 1. */
+fa_status fa_bwd_host(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* d_o, void* dq, void* dk, void* dv, int B,
+                      int Hq, int Hkv, int T, int d, float scale, int causal, int window_left,
+                      int window_right, fa_dtype dtype, int chunks, void* workspace,
+                      unsigned long long workspace_bytes, void* stream);
+
+/* Bytes of device workspace fa_bwd_host needs; 0 for invalid arguments. */
+unsigned long long fa_bwd_host_workspace_size(int B, int Hq, int Hkv, int T, int d,
+                                              fa_dtype dtype, int chunks);
+
 /* Static English text for a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -61,3 +61,24 @@ def test_host_forward_rejects_bad_arguments(cuda_lib):
     assert fa.fa_fwd_host(*args, 0, ws, need) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_host(*args, 2, ws, need - 16) == fa.FA_ERR_WORKSPACE
     assert fa.fa_fwd_host(*args, 2, 0, need) == fa.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("chunks,window", [(1, None), (2, (40, 0)), (3, None), (8, (16, 16))])
+def test_host_backward_matches_device_backward(cuda_lib, chunks, window, dtype):
+    from exact_attention_90_gb300.inputs import make_grad_out
+
+    fa = cuda_lib
+    B, Hq, Hkv, T, d = 5, 4, 2, 300, 64
+    q, k, v = make_qkv(B, Hq, Hkv, T, d, dtype=dtype, seed=54)
+    do = make_grad_out(B, Hq, T, d, dtype=dtype, seed=54)
+    qc, kc, vc, doc = (x.cuda() for x in (q, k, v, do))
+    o, lse = fa.fwd(qc, kc, vc, causal=True, window=window)
+    ref = fa.bwd(qc, kc, vc, o, lse, doc, causal=True, window=window)
+    torch.cuda.synchronize()
+    pinned = [x.pin_memory() for x in (q, k, v, o.cpu(), lse.cpu(), do)]
+    got = fa.bwd_host(*pinned, causal=True, window=window, chunks=chunks)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b.cpu())
