@@ -244,7 +244,9 @@ unsigned long long fa_bwd_local_global_workspace_size(int B, int Hq, int T);
  * overlap kernels.  The work is ordered after everything already on `stream`
  * and everything later on `stream` is ordered after it; the call returns
  * without synchronising (the host outputs are complete once `stream` has
- * reached this point).  Calls on one device run on the GPU in turn.
+ * reached this point).  Calls on one device run on the GPU in turn.  The
+ * first call on a device creates the two streams and three events (kept
+ * until the process exits); make it before any stream capture.
  *   chunks    : 1 .. B (larger values are clamped to B); each chunk should
  *               keep the GPU busy (B*Hq*ceil(T/256)/chunks work units of 256
  *               rows against the number of SMs)
