@@ -23,19 +23,22 @@
 //   warps 4-7 : the same for Q1
 //   warp 8    : TMA producer (Q0, Q1 once; K_j and V_j through rings of
 //               NSK and NSV stages, released separately)
-//   warp 9    : MMA issuer (one thread)
-//   warps 10-11 complete the third warpgroup, whose registers setmaxnreg
-//   hands to the two softmax warpgroups
+//   warp 9    : MMA issuer for Q0 (one thread)
+//   warp 10   : MMA issuer for Q1 (one thread)
+//   warp 11 completes the third warpgroup, whose registers setmaxnreg hands
+//   to the two softmax warpgroups
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  fp32 scores of Q0 K_j^T, Q1 K_j^T
 //   P0, P1      bf16 probabilities packed two per column in the first 64
 //               columns of S0 / S1 (written by the softmax warps)
 //   O0 [256,256+d)  O1 [384,384+d)  fp32 output accumulators
-// Per KV tile j the MMA thread issues  PV0_j, S0_{j+1}, PV1_j, S1_{j+1}; while
-// the tensor core runs one tile's PV and next S, the other tile's softmax
-// warps turn their S into P.  S_{t,j+1} overwrites the columns of P_{t,j};
-// it is issued after PV_{t,j} by the same thread, and tcgen05 MMAs of one
-// thread execute in issue order.
+// Per KV tile j the MMAs go out in the order PV0_j, S0_{j+1}, PV1_j, S1_{j+1};
+// while the tensor core runs one tile's PV and next S, the other tile's
+// softmax warps turn their S into P.  Each Q tile has its own issuing thread
+// and the two hand a turn word back and forth, so that one thread's waits and
+// commits overlap the other's MMAs.  S_{t,j+1} overwrites the columns of
+// P_{t,j}; it is issued after PV_{t,j} by the same thread, and tcgen05 MMAs
+// of one thread execute in issue order.
 // The softmax works in the log2 domain (scores times scale*log2(e), exp2 on
 // the SFU) and rescales O lazily: the reference maximum is only raised when a
 // row's maximum grows by more than 2^8, so most tiles skip the O correction;
@@ -55,7 +58,7 @@ static __device__ unsigned int g_tc_err;
 // Tuning parameters (compile-time; defaults are the measured best):
 //   FA_TC_REG_SPLIT  -- 1: 384 threads, setmaxnreg moves registers from the
 //                       load/MMA warpgroup to the softmax warpgroups;
-//                       0: 320 threads, one register budget for all warps
+//                       0: 352 threads, one register budget for all warps
 #ifndef FA_TC_REG_SPLIT
 #define FA_TC_REG_SPLIT 1
 #endif
@@ -82,13 +85,16 @@ struct TcCfg : TcTile<D> {
   // arrive early; at d = 128: Q 64 KB + K 3 x 32 KB + V 2 x 32 KB = 224 KB.
   static constexpr int NSK = D == 128 ? FA_TC_K_STAGES_D128 : 4;
   static constexpr int NSV = D == 128 ? 2 : 4;
-  static constexpr int THREADS = FA_TC_REG_SPLIT ? 384 : 320;  // softmax Q0, Q1; load/MMA
+  static constexpr int THREADS = FA_TC_REG_SPLIT ? 384 : 352;  // softmax Q0, Q1; load/MMA
   static constexpr int REGS_SOFTMAX = 200;  // per thread after setmaxnreg, warpgroups 0 and 1
   static constexpr int REGS_OTHER = 88;     // warpgroup 2
   // registers the three warpgroups hold after reallocation
   static constexpr int REGS_SPLIT = FA_TC_REG_SPLIT ? 128 * (2 * REGS_SOFTMAX + REGS_OTHER) : 0;
   static constexpr int SMEM_BYTES = 1024 + (2 + NSK + NSV) * Tile::TILE_BYTES + 512;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
+  // the 512 bytes after the tiles: the barriers, the TMEM address, the abort
+  // flag and the issue-turn word
+  static_assert((2 + 2 * NSK + 2 * NSV + 7) * 8 + 3 * 4 <= 512, "barrier area exceeded");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
 };
@@ -235,7 +241,7 @@ enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskBand = 2, kMaskLocalGlobal = 3
 
 // F16: fp16 operands and output (else bf16); accumulation is fp32 either way
 template <int D, int MASK, bool F16>
-__global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
+__global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
@@ -266,6 +272,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     uint64_t *qfull, *qempty, *kfull, *vfull, *kempty, *vempty, *sfull, *pfull, *odone, *final_;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
+    volatile int* turn;  // MMA issue turn of the two issuing threads
     __device__ __forceinline__ explicit Smem(uint8_t* raw) {
       uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -274,17 +281,18 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
       sV = sK + NSK * TILE;     // NSV V tiles
       uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NSV * TILE);
       qfull = bars;             // Q0, Q1 of a unit loaded
-      qempty = bars + 1;        // the unit's last S MMA is done
+      qempty = bars + 1;        // both issuers' last S MMAs of the unit are done
       kfull = bars + 2;
       vfull = kfull + NSK;
-      kempty = vfull + NSV;     // K stage free: its last S MMA is done
-      vempty = kempty + NSK;    // V stage free: its last P.V MMA is done
+      kempty = vfull + NSV;     // K stage free: both issuers are past its S MMAs
+      vempty = kempty + NSK;    // V stage free: both issuers are past its P.V MMAs
       sfull = vempty + NSV;     // [2]
       pfull = sfull + 2;        // [2]
       odone = pfull + 2;        // [2]
       final_ = odone + 2;
       tmem_slot = reinterpret_cast<uint32_t*>(final_ + 1);
       abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+      turn = abort_flag + 1;
     }
   };
 
@@ -298,23 +306,25 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
              *bar_sfull = m.sfull, *bar_pfull = m.pfull, *bar_odone = m.odone,
              *bar_final = m.final_;
     volatile int* abort_flag = m.abort_flag;
+    // the release barriers take one commit from each of the two MMA issuers
     ptx::mbar_init(bar_qfull, 1);
-    ptx::mbar_init(bar_qempty, 1);
+    ptx::mbar_init(bar_qempty, 2);
     for (int s = 0; s < NSK; ++s) {
       ptx::mbar_init(&bar_kfull[s], 1);
-      ptx::mbar_init(&bar_kempty[s], 1);
+      ptx::mbar_init(&bar_kempty[s], 2);
     }
     for (int s = 0; s < NSV; ++s) {
       ptx::mbar_init(&bar_vfull[s], 1);
-      ptx::mbar_init(&bar_vempty[s], 1);
+      ptx::mbar_init(&bar_vempty[s], 2);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&bar_sfull[t], 1);
       ptx::mbar_init(&bar_pfull[t], 4);  // one elected lane per softmax warp
       ptx::mbar_init(&bar_odone[t], 1);
     }
-    ptx::mbar_init(bar_final, 1);
+    ptx::mbar_init(bar_final, 2);
     *abort_flag = 0;
+    *m.turn = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -410,18 +420,48 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
           drain_bar(&bar_vfull[c % NSV], (c / NSV) & 1, &g_tc_err);
       }
       __syncwarp();
-    } else if (warp == 9) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 9 || warp == 10) {
+      // ---------------------------------------------------------- MMA issuers
+      // One thread per Q tile (warp 9: Q0, warp 10: Q1).  The MMA groups keep
+      // the order PV0_j S0_{j+1} | PV1_j S1_{j+1} | PV0_{j+1} ... through a
+      // turn word: a thread waits for its P tile and its loads first, takes
+      // its turn, issues its group, passes the turn, and only then commits,
+      // so its commits and waits overlap the other thread's MMAs.  (Two
+      // independent issuers let the tiles fall into step and their softmax
+      // warpgroups contend; the alternation keeps them half a step apart.)
       if (lane == 0) {
+        const int t = warp - 9;
         constexpr uint32_t IDESC_QK = ptx::idesc_16bit(128, 128, false, false, F16);
         constexpr uint32_t IDESC_PV = ptx::idesc_16bit(128, D, false, true, F16);
         const uint32_t aQ = ptx::smem_u32(sQ);
         const uint32_t aK = ptx::smem_u32(sK);
         const uint32_t aV = ptx::smem_u32(sV);
-        int kc = 0, vc = 0;              // K, V tiles consumed so far
-        int pcnt0 = 0, pcnt1 = 0;        // P tiles consumed so far, per Q tile
-        int nu = 0;                      // units processed so far
+        const uint32_t qlo = Tile::kmajor_lo(aQ + t * TILE);
+        volatile int* turn = m.turn;
+        int kc = 0, vc = 0;  // K, V tiles consumed so far
+        int pc = 0;          // P tiles of this Q tile consumed so far
+        int nu = 0;          // units processed so far
+        int ng = 0;          // turns taken so far
         bool ok = true;
+        // bounded wait for this thread's turn (2 ng + t)
+        auto take_turn = [&]() -> bool {
+          const int want = 2 * ng + t;
+          if (*turn == want) return true;
+          const long long t0 = clock64();
+          while (*turn != want) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > FA_WAIT_BUDGET_CYCLES) {
+              *abort_flag = 1;
+              atomicOr(&g_tc_err, kErrWaitMma);
+              return false;
+            }
+          }
+          return true;
+        };
+        auto pass_turn = [&]() {
+          *turn = 2 * ng + t + 1;
+          ++ng;
+        };
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
@@ -430,77 +470,60 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
           if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
           ++nu;
           ptx::tc_fence_after();
-
-          // tile t is active at local KV tile j when s_t <= j < e_t
-          auto active = [&](int t, int j) {
-            return t == 0 ? (j >= u.s0 && j < u.e0) : (j >= u.s1 && j < u.e1);
-          };
-
-          // S_t = Q_t K_j^T; on an abort no further MMA is issued (the ones in
-          // flight are drained below)
-          auto issue_s = [&](int t, int j) -> bool {
-            const int c = kc + j;
-            const int st = c % NSK;
-            if (!wait_bar(&bar_kfull[st], (c / NSK) & 1, abort_flag, &g_tc_err, kErrWaitMma))
-              return false;
-            ptx::tc_fence_after();
-            const uint32_t qlo = Tile::kmajor_lo(aQ + t * TILE);
-            const uint32_t klo = Tile::kmajor_lo(aK + st * TILE);
-#pragma unroll
-            for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
-              ptx::mma_ss_lh(tmem + C::COL_S0 + t * 128, qlo + Tile::kmajor_step(kk),
-                             Tile::DESC_HI, klo + Tile::kmajor_step(kk), Tile::DESC_HI, IDESC_QK,
-                             kk > 0 ? 1u : 0u);
-            ptx::mma_commit(&bar_sfull[t]);
-            // the last S of KV tile j releases its K stage (tile 1's, when
-            // active, comes after tile 0's); the unit's last S releases Q
-            if (t == 1 || !active(1, j)) ptx::mma_commit(&bar_kempty[st]);
-            if (j == u.cnt - 1 && (t == 1 || !active(1, j))) ptx::mma_commit(bar_qempty);
-            return true;
-          };
-
-          if (ok && active(0, 0)) ok = issue_s(0, 0);
-          if (ok && active(1, 0)) ok = issue_s(1, 0);
-          for (int j = 0; ok && j < u.cnt; ++j) {
-            const int c = vc + j;
-            const int sv = c % NSV;
-            if (!wait_bar(&bar_vfull[sv], (c / NSV) & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
+          const int js = t == 0 ? u.s0 : u.s1;
+          const int je = t == 0 ? u.e0 : u.e1;
+          // one turn per step: [P.V_t(j) when this tile visits KV tile j]
+          // [S_t(j+1) when it visits j+1]; step -1 holds only S_t(0)
+          for (int j = -1; ok && j < u.cnt; ++j) {
+            const bool pv = j >= 0 && j >= js && j < je;
+            const bool sn = j + 1 < u.cnt && j + 1 >= js && j + 1 < je;
+            const int cv = vc + j, ck = kc + j + 1;
+            // the loads are waited for by both threads even when the tile is
+            // not theirs: a release commit before the load has landed would
+            // count towards the stage's previous phase
+            if (j >= 0 && !wait_bar(&bar_vfull[cv % NSV], (cv / NSV) & 1, abort_flag, &g_tc_err,
+                                    kErrWaitMma)) {
+              ok = false;
+              break;
+            }
+            if (j + 1 < u.cnt && !wait_bar(&bar_kfull[ck % NSK], (ck / NSK) & 1, abort_flag,
+                                           &g_tc_err, kErrWaitMma)) {
+              ok = false;
+              break;
+            }
+            if (pv && !wait_bar(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
+              ok = false;
+              break;
+            }
+            if (!take_turn()) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
+            if (pv) {
+              ++pc;
+              const uint32_t vlo = Tile::mnmajor_lo(aV + (cv % NSV) * TILE);
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (ok && active(t, j)) {
-                int& pc = t == 0 ? pcnt0 : pcnt1;
-                if (!wait_bar(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
-                  ok = false;
-                  break;
-                }
-                ++pc;
-                ptx::tc_fence_after();
-                const int first = t == 0 ? u.s0 : u.s1;
-                const uint32_t vlo = Tile::mnmajor_lo(aV + sv * TILE);
+              for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
+                ptx::mma_ts_lh(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
+                               vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
+                               (j > js || kk > 0) ? 1u : 0u);
+            }
+            if (sn) {
+              const uint32_t klo = Tile::kmajor_lo(aK + (ck % NSK) * TILE);
 #pragma unroll
-                for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
-                  ptx::mma_ts_lh(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
-                                 vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
-                                 (j > first || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(&bar_odone[t]);
-                if (t == 1 || !active(1, j)) ptx::mma_commit(&bar_vempty[sv]);
-              }
-              if (ok && active(t, j + 1)) ok = issue_s(t, j + 1);
+              for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
+                ptx::mma_ss_lh(tmem + C::COL_S0 + t * 128, qlo + Tile::kmajor_step(kk),
+                               Tile::DESC_HI, klo + Tile::kmajor_step(kk), Tile::DESC_HI,
+                               IDESC_QK, kk > 0 ? 1u : 0u);
             }
-            if (MASK == kMaskBand && ok && !active(0, j) && !active(1, j)) {
-              // a KV tile neither Q tile needs (a band keeps every row's
-              // diagonal key, so this does not occur): still release both
-              // stages once loaded, so the producer never waits on them
-              const int ck = kc + j;
-              ok = wait_bar(&bar_kfull[ck % NSK], (ck / NSK) & 1, abort_flag, &g_tc_err,
-                            kErrWaitMma);
-              ptx::mma_commit(&bar_kempty[ck % NSK]);
-              ptx::mma_commit(&bar_vempty[sv]);
-            }
+            pass_turn();
+            if (sn) ptx::mma_commit(&bar_sfull[t]);
+            if (pv && j == je - 1) ptx::mma_commit(&bar_odone[t]);
+            if (j >= 0) ptx::mma_commit(&bar_vempty[cv % NSV]);
+            if (j + 1 < u.cnt) ptx::mma_commit(&bar_kempty[ck % NSK]);
+            // Q is free once this thread's last S of the unit is issued
+            if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit(bar_qempty);
           }
           kc += u.cnt;
           vc += u.cnt;
@@ -527,6 +550,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
     const bool neg = scale_log2 < 0.f;
     const float mask_val = neg ? INFINITY : -INFINITY;
     int it = 0;  // S tiles of this Q tile processed so far (barrier phases)
+    int ne = 0;  // epilogues of this Q tile so far (O-done phases)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
@@ -673,7 +697,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 320, 1)
 
       // ---- epilogue: O = O / l in bf16, L = m + ln l (the tensor core meanwhile
       // computes the next unit's first S tiles)
-      ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (it - 1) & 1, abort_flag, &g_tc_err,
+      ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (ne++) & 1, abort_flag, &g_tc_err,
                                             kErrWaitEpilogue));
       if (!ok) break;
       ptx::tc_fence_after();
