@@ -21,8 +21,10 @@
 // Warp roles:
 //   warps 0-3 : softmax, correction and epilogue for Q0 (one thread per row)
 //   warps 4-7 : the same for Q1
-//   warp 8    : TMA producer (Q0, Q1 once; K_j and V_j through rings of
-//               NSK and NSV stages, released separately)
+//   warp 8    : TMA producer (Q tiles through a ring of three slots, so
+//               that the next unit's Q0 is loaded while this unit runs; K_j
+//               and V_j through rings of NSK and NSV stages, released
+//               separately)
 //   warp 9    : MMA issuer for Q0 (one thread)
 //   warp 10   : MMA issuer for Q1 (one thread)
 //   warp 11 completes the third warpgroup, whose registers setmaxnreg hands
@@ -81,8 +83,8 @@ template <int D>
 struct TcCfg : TcTile<D> {
   using Tile = TcTile<D>;
   // K and V ring depths.  K is free once both S MMAs of its tile are done,
-  // V only after both P.V MMAs, so a deeper K ring lets the next K tiles
-  // arrive early; at d = 128: Q 64 KB + K 3 x 32 KB + V 2 x 32 KB = 224 KB.
+  // V only after both P.V MMAs.  At d = 128: Q 3 x 32 KB + K 2 x 32 KB +
+  // V 2 x 32 KB = 224 KB.
   static constexpr int NSK = D == 128 ? FA_TC_K_STAGES_D128 : 4;
   static constexpr int NSV = D == 128 ? 2 : 4;
   static constexpr int THREADS = FA_TC_REG_SPLIT ? 384 : 352;  // softmax Q0, Q1; load/MMA
@@ -90,11 +92,12 @@ struct TcCfg : TcTile<D> {
   static constexpr int REGS_OTHER = 88;     // warpgroup 2
   // registers the three warpgroups hold after reallocation
   static constexpr int REGS_SPLIT = FA_TC_REG_SPLIT ? 128 * (2 * REGS_SOFTMAX + REGS_OTHER) : 0;
-  static constexpr int SMEM_BYTES = 1024 + (2 + NSK + NSV) * Tile::TILE_BYTES + 512;
+  static constexpr int NQ = 3;  // Q tile slots: a unit's Q0, Q1 and the next unit's Q0
+  static constexpr int SMEM_BYTES = 1024 + (NQ + NSK + NSV) * Tile::TILE_BYTES + 512;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   // the 512 bytes after the tiles: the barriers, the TMEM address, the abort
   // flag and the issue-turn word
-  static_assert((2 + 2 * NSK + 2 * NSV + 7) * 8 + 3 * 4 <= 512, "barrier area exceeded");
+  static_assert((2 * NQ + 2 * NSK + 2 * NSV + 7) * 8 + 3 * 4 <= 512, "barrier area exceeded");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
 };
@@ -276,13 +279,13 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
     __device__ __forceinline__ explicit Smem(uint8_t* raw) {
       uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-      sQ = sm;                  // Q0, Q1
-      sK = sm + 2 * TILE;       // NSK K tiles
+      sQ = sm;                  // NQ Q tile slots
+      sK = sm + C::NQ * TILE;   // NSK K tiles
       sV = sK + NSK * TILE;     // NSV V tiles
       uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NSV * TILE);
-      qfull = bars;             // Q0, Q1 of a unit loaded
-      qempty = bars + 1;        // both issuers' last S MMAs of the unit are done
-      kfull = bars + 2;
+      qfull = bars;             // [NQ] Q tile of the slot loaded
+      qempty = bars + C::NQ;    // [NQ] the tile's last S MMA is done
+      kfull = bars + 2 * C::NQ;
       vfull = kfull + NSK;
       kempty = vfull + NSV;     // K stage free: both issuers are past its S MMAs
       vempty = kempty + NSK;    // V stage free: both issuers are past its P.V MMAs
@@ -307,8 +310,10 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
              *bar_final = m.final_;
     volatile int* abort_flag = m.abort_flag;
     // the release barriers take one commit from each of the two MMA issuers
-    ptx::mbar_init(bar_qfull, 1);
-    ptx::mbar_init(bar_qempty, 2);
+    for (int s = 0; s < C::NQ; ++s) {
+      ptx::mbar_init(&bar_qfull[s], 1);
+      ptx::mbar_init(&bar_qempty[s], 1);  // only the tile's own issuer reads it
+    }
     for (int s = 0; s < NSK; ++s) {
       ptx::mbar_init(&bar_kfull[s], 1);
       ptx::mbar_init(&bar_kempty[s], 2);
@@ -365,25 +370,31 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         ptx::prefetch_tmap(&tmV);
         const uint64_t pol_kv = ptx::policy_evict_last();
         const uint64_t pol_q = ptx::policy_evict_first();
-        int q_issued = 0, kc = 0, vc = 0;  // Q pairs, K tiles, V tiles loaded so far
+        int q_issued = 0, kc = 0, vc = 0;  // Q, K, V tiles loaded so far
         bool ok = true;
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
           const TcUnit u = unit_at(idx);
           if (u.cnt == 0) continue;
-          // Q of the previous unit is no longer read once its last S is done
-          if (q_issued > 0 &&
-              !wait_bar(bar_qempty, (q_issued - 1) & 1, abort_flag, &g_tc_err, kErrWaitLoad))
-            break;
-          ptx::mbar_arrive_expect_tx(bar_qfull, 2 * TILE);
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
+          // Q tile i (Q0, Q1 of each unit in turn) goes to slot i % NQ once
+          // the tile NQ before it has had its last S MMA.  With three slots
+          // the next unit's Q0 loads while this unit still runs; its Q1,
+          // which takes this unit's Q0 slot, follows the first K and V tiles
+          auto load_q = [&](int t) -> bool {
+            const int sq = q_issued % C::NQ;
+            if (q_issued >= C::NQ && !wait_bar(&bar_qempty[sq], ((q_issued / C::NQ) - 1) & 1,
+                                               abort_flag, &g_tc_err, kErrWaitLoad))
+              return false;
+            ptx::mbar_arrive_expect_tx(&bar_qfull[sq], TILE);
 #pragma unroll
             for (int bx = 0; bx < Tile::NBOX; ++bx)
-              ptx::tma_load_3d_hint(sQ + t * TILE + bx * Tile::BOX_BYTES, &tmQ, bar_qfull, bx * 64,
-                                    u.q0 + 128 * t, u.bh, pol_q);
-          ++q_issued;
+              ptx::tma_load_3d_hint(sQ + sq * TILE + bx * Tile::BOX_BYTES, &tmQ, &bar_qfull[sq],
+                                    bx * 64, u.q0 + 128 * t, u.bh, pol_q);
+            ++q_issued;
+            return true;
+          };
+          if (!load_q(0)) break;
           const int zkv = u.b * Hkv + u.hk;
           for (int jj = 0; jj < u.cnt; ++jj) {
             const int j = tc_tile_of<LG>(u, jj, lg_list);
@@ -410,10 +421,15 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
               ptx::tma_load_3d_hint(sV + sv * TILE + bx * Tile::BOX_BYTES, &tmV, &bar_vfull[sv],
                                     bx * 64, j * 128, zkv, pol_kv);
             ++vc;
+            if (jj == 0 && !load_q(1)) {
+              ok = false;
+              break;
+            }
           }
         }
         // own copies still in flight (only after an abort) land before exit
-        if (q_issued > 0) drain_bar(bar_qfull, (q_issued - 1) & 1, &g_tc_err);
+        for (int c = max(0, q_issued - C::NQ); c < q_issued; ++c)
+          drain_bar(&bar_qfull[c % C::NQ], (c / C::NQ) & 1, &g_tc_err);
         for (int c = max(0, kc - NSK); c < kc; ++c)
           drain_bar(&bar_kfull[c % NSK], (c / NSK) & 1, &g_tc_err);
         for (int c = max(0, vc - NSV); c < vc; ++c)
@@ -436,7 +452,6 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         const uint32_t aQ = ptx::smem_u32(sQ);
         const uint32_t aK = ptx::smem_u32(sK);
         const uint32_t aV = ptx::smem_u32(sV);
-        const uint32_t qlo = Tile::kmajor_lo(aQ + t * TILE);
         volatile int* turn = m.turn;
         int kc = 0, vc = 0;  // K, V tiles consumed so far
         int pc = 0;          // P tiles of this Q tile consumed so far
@@ -467,8 +482,13 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           if (idx >= num_units) break;
           const TcUnit u = unit_at(idx);
           if (u.cnt == 0) continue;
-          if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_tc_err, kErrWaitMma)) break;
+          // this thread's Q tile of the unit: tile 2 nu + t of the Q ring
+          const int sq = (2 * nu + t) % C::NQ;
+          if (!wait_bar(&bar_qfull[sq], ((2 * nu + t) / C::NQ) & 1, abort_flag, &g_tc_err,
+                        kErrWaitMma))
+            break;
           ++nu;
+          const uint32_t qlo = Tile::kmajor_lo(aQ + sq * TILE);
           ptx::tc_fence_after();
           const int js = t == 0 ? u.s0 : u.s1;
           const int je = t == 0 ? u.e0 : u.e1;
@@ -523,7 +543,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             if (j >= 0) ptx::mma_commit(&bar_vempty[cv % NSV]);
             if (j + 1 < u.cnt) ptx::mma_commit(&bar_kempty[ck % NSK]);
             // Q is free once this thread's last S of the unit is issued
-            if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit(bar_qempty);
+            if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit(&bar_qempty[sq]);
           }
           kc += u.cnt;
           vc += u.cnt;
