@@ -35,7 +35,9 @@
 //   TMEM: S [0,128) [128,256), dP [256,384), dQ [384,384+d).
 //
 // Both grids are persistent (one CTA per SM), units dealt in zig-zag rounds
-// longest first; warps 0-3 compute, warp 4 loads (TMA), warp 5 issues MMAs.
+// longest first; warps 0-3 compute, warp 4 loads (TMA), warp 5 issues MMAs
+// (all 32 lanes run its loop so that operands stay warp-uniform; one elected
+// lane issues).
 // Every wait is bounded (wait.cuh); on expiry the kernel records an error bit,
 // drains its own copies and MMAs, frees tensor memory and exits.
 #include <cmath>
@@ -66,6 +68,12 @@ __device__ __forceinline__ void mask_window(int window_left, int window_right, i
   constexpr bool kBand = MASK == kBwdMaskBand || MASK == kBwdMaskLocalGlobal;
   wl = kBand ? window_left : -1;
   wr = kBand ? window_right : (MASK == kBwdMaskCausal ? 0 : -1);
+}
+
+// a bounded barrier wait by every lane of a warp, with a warp-uniform result
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned int* err, unsigned int code) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err, code));
 }
 
 // ============================================================ dK, dV kernel
@@ -250,7 +258,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the issue loop (its branches are warp-uniform:
+    // every wait ends in a vote); one elected lane issues the MMAs and
+    // commits, so that descriptors and addresses stay warp-uniform values
+    {
       const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
       const uint32_t aStage = ptx::smem_u32(sStage);
       int nu = 0, gs = 0;  // units, query steps issued so far
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dV += P^T dO_s and dK += dS^T Q_s for step s (first: the unit's first step)
       auto grad = [&](int s, int first) -> bool {
         const int bb = s & 1, st = s % NQS;
-        if (!wait_bar(&bar_pfull[bb], (s >> 1) & 1, abort_flag, &g_bwd_err, kErrWaitMma))
+        if (!wait_all(&bar_pfull[bb], (s >> 1) & 1, abort_flag, &g_bwd_err, kErrWaitMma))
           return false;
         ptx::tc_fence_after();
         const uint32_t q_lo = TQ::mnmajor_lo(aStage + st * C::STAGE);
@@ -266,12 +277,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < TQ::PV_KSTEPS; ++kk) {
           const uint32_t acc = (s > first || kk > 0) ? 1u : 0u;
-          ptx::mma_ts_lh(tmem + C::COL_DV, tmem + C::COL_S + bb * 64 + kk * 8,
+          ptx::mma_ts_lh_e(tmem + C::COL_DV, tmem + C::COL_S + bb * 64 + kk * 8,
                          do_lo + TQ::mnmajor_step(kk), TQ::DESC_HI, IDESC_G, acc);
-          ptx::mma_ts_lh(tmem + C::COL_DK, tmem + C::COL_DP + bb * 64 + kk * 8,
+          ptx::mma_ts_lh_e(tmem + C::COL_DK, tmem + C::COL_DP + bb * 64 + kk * 8,
                          q_lo + TQ::mnmajor_step(kk), TQ::DESC_HI, IDESC_G, acc);
         }
-        ptx::mma_commit(&bar_qempty[st]);
+        ptx::mma_commit_e(&bar_qempty[st]);
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -282,14 +293,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if constexpr (LG) kv_query_range_lg(j * 128, T, wl, wr, lg_bits, lg_causal, qlo, qhi);
         else kv_query_range(j * 128, T, wl, wr, qlo, qhi);
         const int nsteps = group * (qhi - qlo);
-        if (!wait_bar(bar_kvfull, nu & 1, abort_flag, &g_bwd_err, kErrWaitMma)) break;
+        if (!wait_all(bar_kvfull, nu & 1, abort_flag, &g_bwd_err, kErrWaitMma)) break;
         ++nu;
         ptx::tc_fence_after();
         const int first = gs;
         const uint32_t k_lo = TK::kmajor_lo(aK), v_lo = TK::kmajor_lo(aV);
         for (int i = 0; i < nsteps; ++i) {
           const int st = gs % NQS, bb = gs & 1;
-          if (!wait_bar(&bar_qfull[st], (gs / NQS) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
+          if (!wait_all(&bar_qfull[st], (gs / NQS) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
             ok = false;
             break;
           }
@@ -298,12 +309,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t do_lo = TQ::kmajor_lo(aStage + st * C::STAGE + TQ::TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < TK::QK_KSTEPS; ++kk) {
-            ptx::mma_ss_lh(tmem + C::COL_S + bb * 64, k_lo + TK::kmajor_step(kk), TK::DESC_HI,
+            ptx::mma_ss_lh_e(tmem + C::COL_S + bb * 64, k_lo + TK::kmajor_step(kk), TK::DESC_HI,
                            q_lo + TQ::kmajor_step(kk), TQ::DESC_HI, IDESC_ST, kk > 0 ? 1u : 0u);
-            ptx::mma_ss_lh(tmem + C::COL_DP + bb * 64, v_lo + TK::kmajor_step(kk), TK::DESC_HI,
+            ptx::mma_ss_lh_e(tmem + C::COL_DP + bb * 64, v_lo + TK::kmajor_step(kk), TK::DESC_HI,
                            do_lo + TQ::kmajor_step(kk), TQ::DESC_HI, IDESC_ST, kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&bar_sfull[bb]);
+          ptx::mma_commit_e(&bar_sfull[bb]);
           if (gs > first && !grad(gs - 1, first)) {
             ok = false;
             break;
@@ -311,10 +322,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ++gs;
         }
         if (ok && nsteps > 0) ok = grad(gs - 1, first);
-        ptx::mma_commit(bar_kvempty);
-        ptx::mma_commit(bar_dkv);
+        ptx::mma_commit_e(bar_kvempty);
+        ptx::mma_commit_e(bar_dkv);
       }
-      ptx::mma_commit(bar_final);
+      ptx::mma_commit_e(bar_final);
       drain_bar(bar_final, 0, &g_bwd_err);
     }
     __syncwarp();
@@ -650,7 +661,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the issue loop (its branches are warp-uniform:
+    // every wait ends in a vote); one elected lane issues the MMAs and
+    // commits, so that descriptors and addresses stay warp-uniform values
+    {
       const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO);
       const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
       int nu = 0, gs = 0;  // units, KV tiles issued so far (one K and one V per tile)
@@ -658,16 +672,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dQ += dS_s K_s for KV tile s (first: the unit's first tile)
       auto grad = [&](int s, int first) -> bool {
         const int bb = s & 1;
-        if (!wait_bar(&bar_pfull[bb], (s >> 1) & 1, abort_flag, &g_bwd_err, kErrWaitMma))
+        if (!wait_all(&bar_pfull[bb], (s >> 1) & 1, abort_flag, &g_bwd_err, kErrWaitMma))
           return false;
         ptx::tc_fence_after();
         const uint32_t k_lo = TT::mnmajor_lo(aK + (s % NSK) * TILE);
 #pragma unroll
         for (int kk = 0; kk < TT::PV_KSTEPS; ++kk)
-          ptx::mma_ts_lh(tmem + C::COL_DQ, tmem + C::COL_S + bb * 128 + kk * 8,
+          ptx::mma_ts_lh_e(tmem + C::COL_DQ, tmem + C::COL_S + bb * 128 + kk * 8,
                          k_lo + TT::mnmajor_step(kk), TT::DESC_HI, IDESC_DQ,
                          (s > first || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(&bar_kempty[s % NSK]);
+        ptx::mma_commit_e(&bar_kempty[s % NSK]);
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -675,14 +689,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (idx >= num_units) break;
         int q0, bh, lo, hi, cnt, nb, ia;
         unit_of(idx, q0, bh, lo, hi, cnt, nb, ia);
-        if (!wait_bar(bar_qfull, nu & 1, abort_flag, &g_bwd_err, kErrWaitMma)) break;
+        if (!wait_all(bar_qfull, nu & 1, abort_flag, &g_bwd_err, kErrWaitMma)) break;
         ++nu;
         ptx::tc_fence_after();
         const int first = gs;
         const uint32_t q_lo = TT::kmajor_lo(aQ), do_lo = TT::kmajor_lo(adO);
         for (int jj = 0; jj < cnt; ++jj) {
           const int bb = gs & 1, sk = gs % NSK, sv = gs % NSV;
-          if (!wait_bar(&bar_kfull[sk], (gs / NSK) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
+          if (!wait_all(&bar_kfull[sk], (gs / NSK) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
             ok = false;
             break;
           }
@@ -690,15 +704,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t k_lo = TT::kmajor_lo(aK + sk * TILE);
 #pragma unroll
           for (int kk = 0; kk < TT::QK_KSTEPS; ++kk)
-            ptx::mma_ss_lh(tmem + C::COL_S + bb * 128, q_lo + TT::kmajor_step(kk), TT::DESC_HI,
+            ptx::mma_ss_lh_e(tmem + C::COL_S + bb * 128, q_lo + TT::kmajor_step(kk), TT::DESC_HI,
                            k_lo + TT::kmajor_step(kk), TT::DESC_HI, IDESC_S, kk > 0 ? 1u : 0u);
           // the dP columns are free once the compute warps have read the last dP
           if (gs > 0 &&
-              !wait_bar(bar_dpfree, (gs - 1) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
+              !wait_all(bar_dpfree, (gs - 1) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
             ok = false;
             break;
           }
-          if (!wait_bar(&bar_vfull[sv], (gs / NSV) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
+          if (!wait_all(&bar_vfull[sv], (gs / NSV) & 1, abort_flag, &g_bwd_err, kErrWaitMma)) {
             ok = false;
             break;
           }
@@ -706,10 +720,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t v_lo = TT::kmajor_lo(aV + sv * TILE);
 #pragma unroll
           for (int kk = 0; kk < TT::QK_KSTEPS; ++kk)
-            ptx::mma_ss_lh(tmem + C::COL_DP, do_lo + TT::kmajor_step(kk), TT::DESC_HI,
+            ptx::mma_ss_lh_e(tmem + C::COL_DP, do_lo + TT::kmajor_step(kk), TT::DESC_HI,
                            v_lo + TT::kmajor_step(kk), TT::DESC_HI, IDESC_S, kk > 0 ? 1u : 0u);
-          ptx::mma_commit(&bar_vempty[sv]);
-          ptx::mma_commit(&bar_sfull[bb]);
+          ptx::mma_commit_e(&bar_vempty[sv]);
+          ptx::mma_commit_e(&bar_sfull[bb]);
           if (gs > first && !grad(gs - 1, first)) {
             ok = false;
             break;
@@ -717,10 +731,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ++gs;
         }
         if (ok && cnt > 0) ok = grad(gs - 1, first);
-        ptx::mma_commit(bar_qempty);
-        ptx::mma_commit(bar_dq);
+        ptx::mma_commit_e(bar_qempty);
+        ptx::mma_commit_e(bar_dq);
       }
-      ptx::mma_commit(bar_final);
+      ptx::mma_commit_e(bar_final);
       drain_bar(bar_final, 0, &g_bwd_err);
     }
     __syncwarp();

@@ -25,8 +25,11 @@
 //               that the next unit's Q0 is loaded while this unit runs; K_j
 //               and V_j through rings of NSK and NSV stages, released
 //               separately)
-//   warp 9    : MMA issuer for Q0 (one thread)
-//   warp 10   : MMA issuer for Q1 (one thread)
+//   warp 9    : MMA issuer for Q0
+//   warp 10   : MMA issuer for Q1
+//   (each issuer warp runs its loop on all 32 lanes, so that descriptors
+//   and addresses stay warp-uniform values; one elected lane issues the
+//   MMAs and commits)
 //   warp 11 completes the third warpgroup, whose registers setmaxnreg hands
 //   to the two softmax warpgroups
 // Tensor memory (512 columns x 128 lanes x 32 bit):
@@ -36,11 +39,11 @@
 //   O0 [256,256+d)  O1 [384,384+d)  fp32 output accumulators
 // Per KV tile j the MMAs go out in the order PV0_j, S0_{j+1}, PV1_j, S1_{j+1};
 // while the tensor core runs one tile's PV and next S, the other tile's
-// softmax warps turn their S into P.  Each Q tile has its own issuing thread
-// and the two hand a turn word back and forth, so that one thread's waits and
+// softmax warps turn their S into P.  Each Q tile has its own issuer warp
+// and the two hand a turn word back and forth, so that one issuer's waits and
 // commits overlap the other's MMAs.  S_{t,j+1} overwrites the columns of
-// P_{t,j}; it is issued after PV_{t,j} by the same thread, and tcgen05 MMAs
-// of one thread execute in issue order.
+// P_{t,j}; it is issued after PV_{t,j} by the same thread (the issuer's
+// elected lane), and tcgen05 MMAs of one thread execute in issue order.
 // The softmax works in the log2 domain (scores times scale*log2(e), exp2 on
 // the SFU) and rescales O lazily: the reference maximum is only raised when a
 // row's maximum grows by more than 2^8, so most tiles skip the O correction;
@@ -173,6 +176,13 @@ __device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T
   u.nband = u.cnt;
   u.ia = 0;
   return u;
+}
+
+// a bounded barrier wait by every lane of a warp, with a warp-uniform result
+__device__ __forceinline__ bool tc_wait_all(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag, unsigned int* err,
+                                            unsigned int code) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err, code));
 }
 
 // first index of the sorted list[0, n) whose entry is >= x (n if none)
@@ -438,14 +448,18 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
       __syncwarp();
     } else if (warp == 9 || warp == 10) {
       // ---------------------------------------------------------- MMA issuers
-      // One thread per Q tile (warp 9: Q0, warp 10: Q1).  The MMA groups keep
+      // One issuer per Q tile (warp 9: Q0, warp 10: Q1).  The MMA groups keep
       // the order PV0_j S0_{j+1} | PV1_j S1_{j+1} | PV0_{j+1} ... through a
       // turn word: a thread waits for its P tile and its loads first, takes
       // its turn, issues its group, passes the turn, and only then commits,
       // so its commits and waits overlap the other thread's MMAs.  (Two
       // independent issuers let the tiles fall into step and their softmax
       // warpgroups contend; the alternation keeps them half a step apart.)
-      if (lane == 0) {
+      // The whole warp runs the issue loop (every branch below is warp-
+      // uniform: waits and the turn end in a vote); one elected lane issues
+      // the MMAs and commits.  With the loop in lane 0 alone the operands
+      // were not warp-uniform values and each MMA issued more slowly.
+      {
         const int t = warp - 9;
         constexpr uint32_t IDESC_QK = ptx::idesc_16bit(128, 128, false, false, F16);
         constexpr uint32_t IDESC_PV = ptx::idesc_16bit(128, D, false, true, F16);
@@ -484,7 +498,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           if (u.cnt == 0) continue;
           // this thread's Q tile of the unit: tile 2 nu + t of the Q ring
           const int sq = (2 * nu + t) % C::NQ;
-          if (!wait_bar(&bar_qfull[sq], ((2 * nu + t) / C::NQ) & 1, abort_flag, &g_tc_err,
+          if (!tc_wait_all(&bar_qfull[sq], ((2 * nu + t) / C::NQ) & 1, abort_flag, &g_tc_err,
                         kErrWaitMma))
             break;
           ++nu;
@@ -501,21 +515,21 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             // the loads are waited for by both threads even when the tile is
             // not theirs: a release commit before the load has landed would
             // count towards the stage's previous phase
-            if (j >= 0 && !wait_bar(&bar_vfull[cv % NSV], (cv / NSV) & 1, abort_flag, &g_tc_err,
+            if (j >= 0 && !tc_wait_all(&bar_vfull[cv % NSV], (cv / NSV) & 1, abort_flag, &g_tc_err,
                                     kErrWaitMma)) {
               ok = false;
               break;
             }
-            if (j + 1 < u.cnt && !wait_bar(&bar_kfull[ck % NSK], (ck / NSK) & 1, abort_flag,
+            if (j + 1 < u.cnt && !tc_wait_all(&bar_kfull[ck % NSK], (ck / NSK) & 1, abort_flag,
                                            &g_tc_err, kErrWaitMma)) {
               ok = false;
               break;
             }
-            if (pv && !wait_bar(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
+            if (pv && !tc_wait_all(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
               ok = false;
               break;
             }
-            if (!take_turn()) {
+            if (!__all_sync(0xffffffffu, take_turn())) {
               ok = false;
               break;
             }
@@ -525,7 +539,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
               const uint32_t vlo = Tile::mnmajor_lo(aV + (cv % NSV) * TILE);
 #pragma unroll
               for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
-                ptx::mma_ts_lh(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
+                ptx::mma_ts_lh_e(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
                                vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
                                (j > js || kk > 0) ? 1u : 0u);
             }
@@ -533,22 +547,22 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
               const uint32_t klo = Tile::kmajor_lo(aK + (ck % NSK) * TILE);
 #pragma unroll
               for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
-                ptx::mma_ss_lh(tmem + C::COL_S0 + t * 128, qlo + Tile::kmajor_step(kk),
+                ptx::mma_ss_lh_e(tmem + C::COL_S0 + t * 128, qlo + Tile::kmajor_step(kk),
                                Tile::DESC_HI, klo + Tile::kmajor_step(kk), Tile::DESC_HI,
                                IDESC_QK, kk > 0 ? 1u : 0u);
             }
             pass_turn();
-            if (sn) ptx::mma_commit(&bar_sfull[t]);
-            if (pv && j == je - 1) ptx::mma_commit(&bar_odone[t]);
-            if (j >= 0) ptx::mma_commit(&bar_vempty[cv % NSV]);
-            if (j + 1 < u.cnt) ptx::mma_commit(&bar_kempty[ck % NSK]);
+            if (sn) ptx::mma_commit_e(&bar_sfull[t]);
+            if (pv && j == je - 1) ptx::mma_commit_e(&bar_odone[t]);
+            if (j >= 0) ptx::mma_commit_e(&bar_vempty[cv % NSV]);
+            if (j + 1 < u.cnt) ptx::mma_commit_e(&bar_kempty[ck % NSK]);
             // Q is free once this thread's last S of the unit is issued
-            if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit(&bar_qempty[sq]);
+            if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit_e(&bar_qempty[sq]);
           }
           kc += u.cnt;
           vc += u.cnt;
         }
-        ptx::mma_commit(bar_final);
+        ptx::mma_commit_e(bar_final);
         drain_bar(bar_final, 0, &g_tc_err);
       }
       __syncwarp();
