@@ -59,7 +59,7 @@ L2_BYTES = 129e6
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # sources of the profiled forward kernel (device code and launch); an ncu
 # summary taken on other sources does not describe it
-KERNEL_SOURCES = ["fa_tc.cu", "ptx.cuh", "tc_layout.cuh", "wait.cuh"]
+KERNEL_SOURCES = ["fa_tc.cu", "ptx.cuh", "tc_layout.cuh", "wait.cuh", "row_store.cuh"]
 
 
 # ---------------------------------------------------------------- helpers

@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_tc.cu", "fa_simt.cu", "fa_unit.cu", "fa_static.cu", "fa_bwd_simt.cu",
            "fa_bwd_tc.cu", "fa_mask.cu", "fa_host.cu"]
-HEADERS = ["ptx.cuh", "tc_layout.cuh", "wait.cuh", "fa_internal.h", "simt_tiles.cuh"]
+HEADERS = ["ptx.cuh", "tc_layout.cuh", "wait.cuh", "row_store.cuh", "fa_internal.h", "simt_tiles.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -44,6 +44,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "row_store.cuh"
 #include "tc_layout.cuh"
 #include "wait.cuh"
 
@@ -416,11 +417,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++nu;
       if (!ok) break;
       ptx::tc_fence_after();
-      const bool row_ok = key < T;
-      const size_t roff = (static_cast<size_t>(bhk) * T + (row_ok ? key : 0)) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        uint16_t* dst_row = (which == 0 ? dV : dK) + roff;
+        // rows of the lane pair, written as whole 32-byte sectors (row_store.cuh)
+        const RowPair rp = row_pair((which == 0 ? dV : dK) + static_cast<size_t>(bhk) * T * D, D,
+                                    key, T, lane);
         const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
         if constexpr (D >= 32) {
 #pragma unroll
@@ -432,12 +433,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int v = 0; v < 16; ++v)
               pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(dst_row + oc * 32);
-#pragma unroll
-              for (int w = 0; w < 4; ++w)
-                dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-            }
+            store_sector_pair(rp, oc * 32, pk);
+            store_sector_pair(rp, oc * 32 + 16, pk + 8);
           }
         } else {
           uint32_t o[16];
@@ -447,11 +444,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int v = 0; v < 8; ++v)
             pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
+          store_sector_pair(rp, 0, pk);
         }
       }
       // the dK, dV reads are complete before this warp releases its next P^T
@@ -825,8 +818,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++nu;
       if (!ok) break;
       ptx::tc_fence_after();
-      const bool row_ok = q < T;
-      uint16_t* dst_row = dQ + (static_cast<size_t>(bh) * T + (row_ok ? q : 0)) * D;
+      // rows of the lane pair, written as whole 32-byte sectors (row_store.cuh)
+      const RowPair rp = row_pair(dQ + static_cast<size_t>(bh) * T * D, D, q, T, lane);
       if constexpr (D >= 32) {
 #pragma unroll
         for (int oc = 0; oc < D / 32; ++oc) {
@@ -837,12 +830,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int v = 0; v < 16; ++v)
             pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + oc * 32);
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-              dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-          }
+          store_sector_pair(rp, oc * 32, pk);
+          store_sector_pair(rp, oc * 32 + 16, pk + 8);
         }
       } else {
         uint32_t o[16];
@@ -852,11 +841,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int v = 0; v < 8; ++v)
           pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+        store_sector_pair(rp, 0, pk);
       }
       ptx::tc_fence_before();
     }

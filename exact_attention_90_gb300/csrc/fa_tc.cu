@@ -53,6 +53,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "row_store.cuh"
 #include "tc_layout.cuh"
 #include "wait.cuh"
 
@@ -770,17 +771,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         ptx::tc_fence_before();
         continue;
       }
-      uint16_t* orow = O + (static_cast<size_t>(u.bh) * T + (row_ok ? grow : 0)) * D;
+      // rows of the lane pair, written as whole 32-byte sectors (row_store.cuh)
+      const RowPair rp = row_pair(O + static_cast<size_t>(u.bh) * T * D, D, grow, T, lane);
       if constexpr (D >= 32) {
-        // Lanes 2i and 2i+1 hold rows r and r+1.  They swap 16-byte pieces so
-        // that each store instruction writes whole 32-byte sectors: the even
-        // lane the first half of a sector, the odd lane the second half, row
-        // r first, then row r+1.
-        const int odd = lane & 1;
-        const int r_even = grow - odd;
-        const bool ok_even = r_even < T, ok_odd = r_even + 1 < T;
-        uint16_t* row_even = O + (static_cast<size_t>(u.bh) * T + (ok_even ? r_even : 0)) * D;
-        uint16_t* row_odd = row_even + (ok_odd ? D : 0);
 #pragma unroll
         for (int oc = 0; oc < D / 32; ++oc) {
           uint32_t o[32];
@@ -791,24 +784,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           for (int v = 0; v < 16; ++v)
             pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * inv_l,
                                       __uint_as_float(o[2 * v + 1]) * inv_l);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {  // the two 32-byte sectors of these 32 columns
-            uint32_t snd[4], rcv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              snd[e] = odd ? pk[8 * h + e] : pk[8 * h + 4 + e];
-              rcv[e] = __shfl_xor_sync(0xffffffffu, snd[e], 1);
-            }
-            const int piece = oc * 32 + (2 * h + odd) * 8;  // element offset in the row
-            if (ok_even)
-              *reinterpret_cast<uint4*>(row_even + piece) =
-                  odd ? make_uint4(rcv[0], rcv[1], rcv[2], rcv[3])
-                      : make_uint4(pk[8 * h], pk[8 * h + 1], pk[8 * h + 2], pk[8 * h + 3]);
-            if (ok_odd)
-              *reinterpret_cast<uint4*>(row_odd + piece) =
-                  odd ? make_uint4(pk[8 * h + 4], pk[8 * h + 5], pk[8 * h + 6], pk[8 * h + 7])
-                      : make_uint4(rcv[0], rcv[1], rcv[2], rcv[3]);
-          }
+          store_sector_pair(rp, oc * 32, pk);
+          store_sector_pair(rp, oc * 32 + 16, pk + 8);
         }
       } else {
         uint32_t o[16];
@@ -819,11 +796,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         for (int v = 0; v < 8; ++v)
           pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * inv_l,
                                     __uint_as_float(o[2 * v + 1]) * inv_l);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+        store_sector_pair(rp, 0, pk);
       }
       if (row_ok)
         LSE[static_cast<size_t>(u.bh) * T + grow] = (m_ref + log2f(l)) * 0.6931471805599453f;
