@@ -103,6 +103,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def alu_peaks(peaks: dict, sms: int) -> dict:
+    """Peaks of the two non-tensor pipes the forward can be bound by, derived
+    from unit counts and the maximum SM clock (``sm_max_mhz`` of the measured
+    peaks, else 2070 MHz):
+      fp32_tflops: SMs x 128 FP32 lanes x 2 flops per FMA x clock (the
+                   true-fp32 CUDA-core kernel is bound by FFMA);
+      exp_per_s:   SMs x 32 ex2 per clock (one warp instruction per 4 clocks
+                   per SMSP, measured on GB300) x clock -- one exponential per
+                   kept (row, key) pair bounds the small-d shapes."""
+    hz = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    return {"fp32_tflops": sms * 128 * 2 * hz / 1e12, "exp_per_s": sms * 32 * hz}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -429,8 +442,12 @@ def run_ours(args, w):
     ms_per = ms / args.steps
     achieved = flops / (ms_per / 1e3) / 1e12
     # fp16 and bf16 share the dense tensor rate (nominal ratio 1:1); the fp32
-    # kernel runs on the CUDA cores and has no tensor peak
-    peak = float(peaks["bf16_tflops"]) if w.dtype in ("bf16", "f16") else None
+    # kernel runs on the CUDA cores, bound by FFMA (alu_peaks)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu = alu_peaks(peaks, sms)
+    tensor_path = w.dtype in ("bf16", "f16")
+    peak = float(peaks["bf16_tflops"]) if tensor_path else alu["fp32_tflops"]
+    pairs = w.flops / (4.0 * w.d)  # kept (row, key) pairs: one exponential each
     traffic = None if bwd else ncu_traffic(w.name)
     clocks = sampler.summary(t_wall0, t_wall1)
 
@@ -446,9 +463,14 @@ def run_ours(args, w):
                 "path": (f"{'fa_bwd_host' if bwd else 'fa_fwd_host'}: pinned host buffers, "
                          f"{chunks} batch chunks pipelined over 2 streams")},
         "gpu_launches": args.steps * (3 if bwd else 1),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (achieved / peak) if peak else None, "traffic": traffic,
-                     "peak_source": f"bf16_tflops (burst) of {src}",
+        "roofline": {"bound": "tensor" if tensor_path else "alu", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": (f"bf16_tflops (burst) of {src}" if tensor_path else
+                                     f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x "
+                                     f"{float(peaks.get('sm_max_mhz', 2070.0)):.0f} MHz"),
+                     "exp_frac": (None if bwd else
+                                  pairs / (ms_per / 1e3) / alu["exp_per_s"]),
                      "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes_per_launch": w.bytes,
                      "hbm_gbs": w.bytes / (ms_per / 1e3) / 1e9,
@@ -483,6 +505,7 @@ def run_all(args):
     fa.load_library()
     peaks, src = load_peaks()
     dev = torch.device("cuda", 0)
+    alu = alu_peaks(peaks, torch.cuda.get_device_properties(dev).multi_processor_count)
     flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
     bwd = args.pass_ == "bwd"
     for w in all_workloads():
@@ -520,6 +543,9 @@ def run_all(args):
         gbs = w.bytes / (ms / 1e3) / 1e9
         print(json.dumps({"workload": w.name, "pass": "bwd" if bwd else "fwd", "ms": ms,
                           "tflops": tf, "frac_bf16_peak": tf / float(peaks["bf16_tflops"]),
+                          "frac_fp32_alu": (tf / alu["fp32_tflops"]) if w.dtype == "f32" else None,
+                          "frac_exp": (None if bwd else
+                                       w.flops / (4.0 * w.d) / (ms / 1e3) / alu["exp_per_s"]),
                           "hbm_gbs": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"]),
                           "peaks": src, "l2": "flushed (256 MB write) before each call"}),
               flush=True)
