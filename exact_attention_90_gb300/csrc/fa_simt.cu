@@ -11,11 +11,14 @@
 // (fp32 arithmetic), which the tests use as a cross-check of the tensor-core
 // kernel.
 //
-// CTA = 128 threads = a 16 x 8 grid (tx, ty) over a 64-query x 64-key block:
-// thread (tx, ty) owns query rows ty*8 .. ty*8+7, score columns tx*4 .. tx*4+3
-// and d/16 output columns; row maxima and sums combine the 16 threads of a row
-// with warp shuffles.  Tiles live in shared memory with padded rows so the
-// 16-byte loads of a quarter-warp hit distinct banks.
+// CTA = 2 FQ threads = a 16 x (FQ / 8) grid (tx, ty) over an FQ-query x
+// 64-key block (FQ = 64 or 128): thread (tx, ty) owns query rows ty*8 ..
+// ty*8+7, score columns tx*4 .. tx*4+3 and d/16 output columns; row maxima
+// and sums combine the 16 threads of a row with warp shuffles.  Tiles live in
+// shared memory with padded rows so the 16-byte loads of a quarter-warp hit
+// distinct banks.  FQ = 128 gives eight warps per SM at d = 128 (the shared
+// memory allows one CTA there) and halves the K/V loads per flop; the host
+// takes it for d >= 64 when the grid still covers every SM.
 #include <cmath>
 
 #include "fa_internal.h"
@@ -31,35 +34,44 @@ using namespace simt;
 // unbounded side); no mask is (-1, -1), causal attention (-1, 0).  With
 // lg_bits (local-global mask: one bit per key) a flagged key is kept as well,
 // up to the row itself when lg_causal.
-template <typename Tin, int D>
-__global__ void __launch_bounds__(128)
+// FQ query rows per CTA, 2 FQ threads (16 per 8 rows x 64 keys)
+template <int D, int FQ>
+struct FwdSimtCfg {
+  static constexpr int FT = 2 * FQ;
+  static constexpr int QS = SimtCfg<D>::QS, PS = SimtCfg<D>::PS, OC = SimtCfg<D>::OC;
+  static constexpr int SMEM_BYTES = (FQ * QS + BK * QS + BK * D + FQ * PS) * 4;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
+};
+
+template <typename Tin, int D, int FQ>
+__global__ void __launch_bounds__(2 * FQ)
     fa_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                        const Tin* __restrict__ v, Tin* __restrict__ o, float* __restrict__ lse,
                        int B, int Hq, int Hkv, int T, float scale, int wl, int wr,
                        const uint32_t* __restrict__ lg_bits, int lg_causal) {
-  using C = SimtCfg<D>;
-  constexpr int QS = C::QS, PS = C::PS, OC = C::OC;
+  using C = FwdSimtCfg<D, FQ>;
+  constexpr int QS = C::QS, PS = C::PS, OC = C::OC, FT = C::FT;
   constexpr int GW = D >= 64 ? 4 : (D == 32 ? 2 : 1);  // contiguous output columns
   extern __shared__ float4 smem4[];
   float* sQ = reinterpret_cast<float*>(smem4);
-  float* sK = sQ + BQ * QS;
+  float* sK = sQ + FQ * QS;
   float* sV = sK + BK * QS;
   float* sP = sV + BK * D;
 
   const int tid = threadIdx.x;
   const int ty = tid >> 4, tx = tid & 15;
   const int BH = B * Hq;
-  const int n_qt = (T + BQ - 1) / BQ;
+  const int n_qt = (T + FQ - 1) / FQ;
   const int n_kt = (T + BK - 1) / BK;
   const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // last (causal: longest) first
   const int bh = static_cast<int>(blockIdx.x % BH);
   const int b = bh / Hq, h = bh - (bh / Hq) * Hq;
   const int hk = h / (Hq / Hkv);
-  const int q0 = qt * BQ;
+  const int q0 = qt * FQ;
   const size_t qoff = static_cast<size_t>(bh) * T * D;
   const size_t kvoff = static_cast<size_t>(b * Hkv + hk) * T * D;
 
-  load_tile<D, QS>(sQ, q + qoff, q0, T);
+  load_tile<D, QS, FQ, FT>(sQ, q + qoff, q0, T);
 
   float m[8], lp[8], acc[8][OC];
 #pragma unroll
@@ -70,20 +82,20 @@ __global__ void __launch_bounds__(128)
     for (int c = 0; c < OC; ++c) acc[i][c] = 0.f;
   }
 
-  // KV blocks holding keys [q0 - wl, q0 + BQ - 1 + wr] of the band, within T
+  // KV blocks holding keys [q0 - wl, q0 + FQ - 1 + wr] of the band, within T
   const int b_lo = wl < 0 ? 0 : max(0, q0 - wl) / BK;
-  const int b_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + BQ - 1 + wr) / BK + 1);
+  const int b_hi = wr < 0 ? n_kt : min(n_kt, min(T - 1, q0 + FQ - 1 + wr) / BK + 1);
   // local-global: global keys may sit in any block (before the rows' last
   // key when causal); blocks with neither band keys nor global keys are skipped
   const int j_lo = lg_bits ? 0 : b_lo;
-  const int j_hi = lg_bits ? (lg_causal ? min(n_kt, min(T - 1, q0 + BQ - 1) / BK + 1) : n_kt)
+  const int j_hi = lg_bits ? (lg_causal ? min(n_kt, min(T - 1, q0 + FQ - 1) / BK + 1) : n_kt)
                            : b_hi;
   for (int j = j_lo; j < j_hi; ++j) {
     if (lg_bits && (j < b_lo || j >= b_hi) && (__ldg(lg_bits + 2 * j) | __ldg(lg_bits + 2 * j + 1)) == 0u)
       continue;
     __syncthreads();  // previous block's K, V, P no longer in use
-    load_tile<D, QS>(sK, k + kvoff, j * BK, T);
-    load_tile<D, D>(sV, v + kvoff, j * BK, T);
+    load_tile<D, QS, BK, FT>(sK, k + kvoff, j * BK, T);
+    load_tile<D, D, BK, FT>(sV, v + kvoff, j * BK, T);
     __syncthreads();
 
     // S = Q K^T for the thread's 8 x 4 scores
@@ -202,10 +214,10 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-template <typename Tin, int D>
+template <typename Tin, int D, int FQ>
 fa_status launch_simt_impl(const FwdArgs& a) {
-  using C = SimtCfg<D>;
-  auto kern = fa_fwd_simt_kernel<Tin, D>;
+  using C = FwdSimtCfg<D, FQ>;
+  auto kern = fa_fwd_simt_kernel<Tin, D, FQ>;
   static bool attr_done[64] = {};  // per instantiation and device; benign race
   bool* done = device_flag(attr_done);
   if (done == nullptr || !*done) {
@@ -214,23 +226,30 @@ fa_status launch_simt_impl(const FwdArgs& a) {
     if (e != cudaSuccess) return cuda_status(e);
     if (done != nullptr) *done = true;
   }
-  const long long blocks = static_cast<long long>(a.B) * a.Hq * ((a.T + BQ - 1) / BQ);
+  const long long blocks = static_cast<long long>(a.B) * a.Hq * ((a.T + FQ - 1) / FQ);
   int wl, wr;
   effective_window(a, wl, wr);
-  kern<<<static_cast<unsigned>(blocks), 128, C::SMEM_BYTES, a.stream>>>(
+  kern<<<static_cast<unsigned>(blocks), C::FT, C::SMEM_BYTES, a.stream>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
       static_cast<Tin*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, a.scale, wl, wr,
       a.local_global ? a.lg_bits : nullptr, a.causal);
   return cuda_status(cudaGetLastError());
 }
 
+// 128-row CTAs (eight warps) for d >= 64 when they still give every SM a CTA;
+// 64-row CTAs otherwise (measured: at d <= 32 and for few (b, h) the smaller
+// CTA is faster)
 template <typename Tin>
 fa_status launch_simt_t(const FwdArgs& a) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool wide = a.d >= 64 && static_cast<long long>(a.B) * a.Hq * ((a.T + 127) / 128) >= sms;
   switch (a.d) {
-    case 16: return launch_simt_impl<Tin, 16>(a);
-    case 32: return launch_simt_impl<Tin, 32>(a);
-    case 64: return launch_simt_impl<Tin, 64>(a);
-    case 128: return launch_simt_impl<Tin, 128>(a);
+    case 16: return launch_simt_impl<Tin, 16, 64>(a);
+    case 32: return launch_simt_impl<Tin, 32, 64>(a);
+    case 64: return wide ? launch_simt_impl<Tin, 64, 128>(a) : launch_simt_impl<Tin, 64, 64>(a);
+    case 128: return wide ? launch_simt_impl<Tin, 128, 128>(a) : launch_simt_impl<Tin, 128, 64>(a);
     default: return FA_ERR_UNSUPPORTED;
   }
 }

@@ -1,6 +1,6 @@
 // simt_tiles.cuh -- shared-memory tile helpers of the fp32 CUDA-core kernels
-// (forward in fa_simt.cu, backward in fa_bwd_simt.cu): 64-row tiles of a
-// [T][D] matrix converted to fp32 in padded shared-memory rows, and
+// (forward in fa_simt.cu, backward in fa_bwd_simt.cu): row tiles of a [T][D]
+// matrix converted to fp32 in padded shared-memory rows, and
 // vectorised stores of fp32 results in the output element type.
 #pragma once
 
@@ -32,13 +32,13 @@ __device__ __forceinline__ int ocol(int tx, int c) {
   else return tx;
 }
 
-// rows [r0, r0+64) of a [T][D] matrix into smem (row stride LS floats); rows
-// at or past T become zero
-template <int D, int LS>
+// rows [r0, r0+ROWS) of a [T][D] matrix into smem (row stride LS floats),
+// by the NT threads of the CTA; rows at or past T become zero
+template <int D, int LS, int ROWS = 64, int NT = 128>
 __device__ __forceinline__ void load_tile(float* dst, const float* src, int r0, int T) {
   constexpr int V = D / 4;  // float4 per row
 #pragma unroll 4
-  for (int idx = threadIdx.x; idx < 64 * V; idx += 128) {
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += NT) {
     const int r = idx / V, c4 = idx % V;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r0 + r < T) x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(r0 + r) * D) + c4);
@@ -46,11 +46,11 @@ __device__ __forceinline__ void load_tile(float* dst, const float* src, int r0, 
   }
 }
 
-template <int D, int LS>
+template <int D, int LS, int ROWS = 64, int NT = 128>
 __device__ __forceinline__ void load_tile(float* dst, const __nv_bfloat16* src, int r0, int T) {
   constexpr int V = D / 8;  // 16-byte vectors of 8 bf16 per row
 #pragma unroll 4
-  for (int idx = threadIdx.x; idx < 64 * V; idx += 128) {
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += NT) {
     const int r = idx / V, c8 = idx % V;
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
     if (r0 + r < T) x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r0 + r) * D) + c8);
@@ -67,11 +67,11 @@ __device__ __forceinline__ void load_tile(float* dst, const __nv_bfloat16* src, 
   }
 }
 
-template <int D, int LS>
+template <int D, int LS, int ROWS = 64, int NT = 128>
 __device__ __forceinline__ void load_tile(float* dst, const __half* src, int r0, int T) {
   constexpr int V = D / 8;  // 16-byte vectors of 8 fp16 per row
 #pragma unroll 4
-  for (int idx = threadIdx.x; idx < 64 * V; idx += 128) {
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += NT) {
     const int r = idx / V, c8 = idx % V;
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
     if (r0 + r < T) x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r0 + r) * D) + c8);

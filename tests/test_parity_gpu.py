@@ -187,6 +187,36 @@ def test_causal_row0_and_zero_query_closed_forms(cuda_lib):
         assert err <= TOL[dtype][1]
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [129, 200, 257])
+def test_full_parity_simt_wide_ctas(cuda_lib, T, d, causal):
+    """The CUDA-core kernel with 128-row CTAs: it takes them for d >= 64 once
+    the grid gives every SM a CTA (here 2 x 76 heads x 2 row blocks = 304),
+    and 64-row CTAs below that, which the small shapes above exercise.  GQA
+    heads and a ragged last block of rows."""
+    q, k, v = make_qkv(2, 76, 38, T, d, dtype="f32", seed=T + d, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run(cuda_lib, q, k, v, causal, scale)
+    check_full(o, lse, q, k, v, scale, causal, what=f"wide T={T} d={d} causal={causal}")
+
+
+def test_simt_wide_ctas_window_and_16bit(cuda_lib):
+    """128-row CTAs with a band window, and on bf16 inputs (fp32 arithmetic)."""
+    fa = cuda_lib
+    q, k, v = make_qkv(2, 76, 76, 300, 128, dtype="f32", seed=12, device="cuda")
+    scale = 1.0 / math.sqrt(128)
+    o, lse = fa.fwd(q, k, v, causal=False, scale=scale, window=(70, 20))
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+    O_ref, L_ref = oracle.attention_ref(q, k, v, scale, False, window=(70, 20))
+    assert float(np.max(np.abs(oracle.as_f64(o) - O_ref))) <= TOL["f32"][0]
+    assert float(np.max(np.abs(oracle.as_f64(lse) - L_ref))) <= TOL["f32"][1]
+    qb, kb, vb = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    o2, l2 = run(fa, qb, kb, vb, True, scale, kernel="simt")
+    check_full(o2, l2, qb, kb, vb, scale, True, what="wide bf16 via the CUDA-core kernel")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_tensor_core_agrees_with_fp32_simt(cuda_lib, dtype):
     """The tcgen05 kernel and the CUDA-core kernel on the same 16-bit inputs."""
