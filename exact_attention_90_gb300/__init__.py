@@ -28,7 +28,8 @@ __all__ = [
     "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_window", "fa_fwd_split",
     "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
-    "fa_fwd_local_global", "fa_fwd_local_global_workspace_size", "fa_bwd_local_global",
+    "fa_fwd_local_global", "fa_fwd_local_global_workspace_size",
+    "fa_fwd_local_global_packed_workspace_size", "fa_bwd_local_global",
     "fa_bwd_local_global_workspace_size", "fa_fwd_host", "fa_fwd_host_workspace_size", "fwd_host",
     "fa_bwd_host", "fa_bwd_host_workspace_size", "bwd_host",
     "bwd", "FA_DTYPE_F32",
@@ -74,6 +75,7 @@ EXPORTS = [
     ("fa_fwd_local_global", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _I, _I,
                                  _P, ctypes.c_ulonglong, _P]),
     ("fa_fwd_local_global_workspace_size", ctypes.c_ulonglong, [_I]),
+    ("fa_fwd_local_global_packed_workspace_size", ctypes.c_ulonglong, [_I, _I, _I, _I, _I, _I]),
     ("fa_bwd_local_global", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
                                  _I, _P, _I, _I, _P, ctypes.c_ulonglong, _P]),
     ("fa_bwd_local_global_workspace_size", ctypes.c_ulonglong, [_I, _I, _I]),
@@ -228,6 +230,11 @@ def fa_fwd_local_global_workspace_size(T) -> int:
     return load_library().fa_fwd_local_global_workspace_size(int(T))
 
 
+def fa_fwd_local_global_packed_workspace_size(B, Hkv, T, d, dtype, num_global) -> int:
+    return load_library().fa_fwd_local_global_packed_workspace_size(
+        int(B), int(Hkv), int(T), int(d), int(dtype), int(num_global))
+
+
 def fa_bwd_local_global(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, T, d, scale, causal,
                         local_window, global_tokens, num_global, dtype, workspace,
                         workspace_bytes, stream=None) -> int:
@@ -326,7 +333,7 @@ def _dtype_code(t) -> int:
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
         stream=None, kernel: str = "auto", num_splits: int | None = None, window=None,
-        global_tokens=None):
+        global_tokens=None, pack_global: bool = True):
     """Attention forward on CUDA tensors; returns (o, lse).
 
     q: [B, Hq, T, d]; k, v: [B, Hkv, T, d]; all contiguous CUDA tensors of one
@@ -342,7 +349,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     the causal mask when ``causal`` is set.  ``global_tokens`` (a CUDA int32
     tensor of key indices) selects the local-global mask: ``window`` must
     then be (w, w) or None (w = 0), and query i keeps key j when |i - j| <= w
-    or j is a global token (intersected with causal).  The call is
+    or j is a global token (intersected with causal).  With ``pack_global``
+    (default) the 16-bit path gathers the global keys into packed tiles (the
+    larger workspace of fa_fwd_local_global_packed_workspace_size); False
+    visits whole key tiles instead (same results).  The call is
     asynchronous on ``stream`` (default: the current torch stream).
     """
     import torch
@@ -374,7 +384,9 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         if (not isinstance(global_tokens, torch.Tensor) or not global_tokens.is_cuda
                 or global_tokens.dtype != torch.int32 or not global_tokens.is_contiguous()):
             raise TypeError("global_tokens must be a contiguous CUDA int32 tensor")
-        nbytes = fa_fwd_local_global_workspace_size(T)
+        nbytes = (fa_fwd_local_global_packed_workspace_size(B, Hkv, T, d, code,
+                                                            global_tokens.numel())
+                  if pack_global else fa_fwd_local_global_workspace_size(T))
         ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
         st = fa_fwd_local_global(q, k, v, out, lse, B, Hq, Hkv, T, d, scale, int(bool(causal)), wl,
                                  global_tokens if global_tokens.numel() else 0,

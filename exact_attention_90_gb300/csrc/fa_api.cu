@@ -162,9 +162,13 @@ fa_status fa_fwd_local_global(const void* q, const void* k, const void* v, void*
   if (reinterpret_cast<uintptr_t>(global_tokens) & 3u) return FA_ERR_MISALIGNED;
   if (workspace == nullptr) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_MISALIGNED;
-  const size_t need = fa::lg_workspace_bytes(T);
-  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const size_t lg_need = fa::lg_workspace_bytes(T);
+  if (workspace_bytes < lg_need) return FA_ERR_WORKSPACE;
   const size_t e = dtype == FA_DTYPE_F32 ? 4 : 2;
+  // packed global keys when the workspace has room (16-bit inputs only)
+  const size_t pack = dtype == FA_DTYPE_F32 ? 0 : fa::lg_pack_workspace_bytes(B, Hkv, d, e, num_global);
+  const bool packed = dtype != FA_DTYPE_F32 && num_global > 0 && workspace_bytes >= lg_need + pack;
+  const size_t need = lg_need + (packed ? pack : 0);
   const size_t nq = static_cast<size_t>(B) * Hq * T * d * e;
   const size_t nkv = static_cast<size_t>(B) * Hkv * T * d * e;
   const size_t nl = static_cast<size_t>(B) * Hq * T * 4;
@@ -177,12 +181,25 @@ fa_status fa_fwd_local_global(const void* q, const void* k, const void* v, void*
     return FA_ERR_INVALID_ARG;
   s = fa::launch_lg_prep(a, global_tokens, num_global, workspace);
   if (s != FA_OK) return s;
+  if (packed) {
+    s = fa::launch_lg_pack(a, num_global, static_cast<uint8_t*>(workspace) + lg_need);
+    if (s != FA_OK) return s;
+  }
   return dtype == FA_DTYPE_F32 ? fa::launch_simt(a) : fa::launch_tc(a);
 }
 
 unsigned long long fa_fwd_local_global_workspace_size(int T) {
   if (T <= 0) return 0;
   return fa::lg_workspace_bytes(T);
+}
+
+unsigned long long fa_fwd_local_global_packed_workspace_size(int B, int Hkv, int T, int d,
+                                                             fa_dtype dtype, int num_global) {
+  if (B <= 0 || Hkv <= 0 || T <= 0 || d <= 0 || num_global < 0) return 0;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_F32) return 0;
+  const size_t lg = fa::lg_workspace_bytes(T);
+  if (dtype == FA_DTYPE_F32 || num_global == 0) return lg;
+  return lg + fa::lg_pack_workspace_bytes(B, Hkv, d, 2, num_global);
 }
 
 fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse, int B,

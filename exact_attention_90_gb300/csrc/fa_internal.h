@@ -33,6 +33,16 @@ struct FwdArgs {
   const uint32_t* lg_bits = nullptr;
   const int* lg_list = nullptr;
   const int* lg_count = nullptr;
+  // packed global keys (16-bit tensor-core path, launch_lg_pack): the sorted
+  // distinct global tokens lg_tokens[0, *lg_ntok) and their K and V rows
+  // gathered into lg_kg, lg_vg, [B*Hkv][lg_rows][d] (lg_rows: a multiple of
+  // 128; rows past the token count are zero)
+  bool lg_packed = false;
+  const int* lg_tokens = nullptr;
+  const int* lg_ntok = nullptr;
+  const void* lg_kg = nullptr;
+  const void* lg_vg = nullptr;
+  int lg_rows = 0;
 };
 
 // Workspace of the local-global mask for T keys: the key bitmask (16 bytes
@@ -51,6 +61,17 @@ fa_status lg_prep(int T, const int* global_tokens, int num_global, void* workspa
                   cudaStream_t stream, LgSets* out);
 // The same for a forward call: points a.lg_* at the sets.
 fa_status launch_lg_prep(FwdArgs& a, const int* global_tokens, int num_global, void* workspace);
+
+// Workspace of the packed global keys on top of lg_workspace_bytes(T): the
+// sorted distinct tokens (lg_pack_rows(num_global) ints), their count, and the
+// K and V rows gathered per (b, KV head): 2 * B * Hkv * rows * d * elem bytes,
+// rows = num_global rounded up to a multiple of 128.
+int lg_pack_rows(int num_global);
+size_t lg_pack_workspace_bytes(int B, int Hkv, int d, size_t elem, int num_global);
+// After launch_lg_prep: compacts the bitmask into the sorted token list and
+// gathers the K, V rows into `pack_ws` (lg_pack_workspace_bytes bytes, 16-byte
+// aligned); sets a.lg_packed and the a.lg_* pointers of the packed keys.
+fa_status launch_lg_pack(FwdArgs& a, int num_global, void* pack_ws);
 
 // The band the kernels apply: the window intersected with causal (j <= i).
 // A side of T - 1 or more reaches every key, so it becomes unbounded (-1):

@@ -136,8 +136,9 @@ struct TcUnit {
   int bh, b, hk, q0, sp, j0, s0, e0, s1, e1, cnt;
   // local-global masks: the unit's KV tiles are the nb global tiles below
   // its band, the nband band tiles from j0 on, then the global tiles from
-  // list index ia on (below, j0 + j is the band's tile for nb = 0)
-  int nb, nband, ia;
+  // list index ia on (below, j0 + j is the band's tile for nb = 0); with
+  // packed global keys: nb = 0, the band tiles, then np packed tiles
+  int nb, nband, ia, np;
 };
 
 __device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T, int S, int wl,
@@ -176,6 +177,7 @@ __device__ __forceinline__ TcUnit tc_unit(int idx, int B, int Hq, int Hkv, int T
   u.nb = 0;
   u.nband = u.cnt;
   u.ia = 0;
+  u.np = 0;
   return u;
 }
 
@@ -202,10 +204,27 @@ __device__ __forceinline__ int tc_lower_bound(const int* list, int n, int x) {
 // uhi up to the last tile any row of the unit may see (its own last row's
 // tile when causal).  Both Q tiles visit every tile of the unit; the mask
 // removes what a row does not see.
+//
+// With packed global keys (`packed`: the sorted distinct tokens gtok[0,
+// *gntok) in 128-row packed K/V tiles) the unit visits its band tiles and
+// then every packed tile holding a token its rows may see (up to its last
+// row when causal): a global key costs a packed row, not a whole tile.
 __device__ __forceinline__ TcUnit tc_unit_lg(int idx, int B, int Hq, int Hkv, int T, int wl,
                                              int wr, int causal, const int* glist,
-                                             const int* gcount) {
+                                             const int* gcount, int packed, const int* gtok,
+                                             const int* gntok) {
   TcUnit u = tc_unit(idx, B, Hq, Hkv, T, 1, wl, wr);
+  if (packed) {
+    const int G = __ldg(gntok);
+    const int g_hi = causal ? tc_lower_bound(gtok, G, min(T - 1, u.q0 + 255) + 1) : G;
+    u.nband = u.cnt;
+    u.np = (g_hi + 127) >> 7;
+    u.cnt = u.nband + u.np;
+    u.s0 = u.s1 = 0;
+    u.e0 = u.q0 < T ? u.cnt : 0;
+    u.e1 = u.q0 + 128 < T ? u.cnt : 0;
+    return u;
+  }
   const int ulo = u.j0, uhi = u.j0 + u.cnt;
   const int n = __ldg(gcount);
   const int cap = causal ? min(T - 1, u.q0 + 255) >> 7 : (T - 1) >> 7;
@@ -263,13 +282,18 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
                      int num_units, int S, float* __restrict__ part_o,
                      float* __restrict__ part_lse, int window_left, int window_right,
                      const uint32_t* __restrict__ lg_bits, const int* __restrict__ lg_list,
-                     const int* __restrict__ lg_count, int lg_causal) {
+                     const int* __restrict__ lg_count, int lg_causal,
+                     const __grid_constant__ CUtensorMap tmKg,
+                     const __grid_constant__ CUtensorMap tmVg, int lg_packed,
+                     const int* __restrict__ lg_tokens, const int* __restrict__ lg_ntok) {
   constexpr bool LG = MASK == kMaskLocalGlobal;
   // the band [i - wl, i + wr] of the mask kind (a negative side: unbounded)
   const int wl = (MASK == kMaskBand || LG) ? window_left : -1;
   const int wr = (MASK == kMaskBand || LG) ? window_right : (MASK == kMaskCausal ? 0 : -1);
   auto unit_at = [&](int idx) {
-    if constexpr (LG) return tc_unit_lg(idx, B, Hq, Hkv, T, wl, wr, lg_causal, lg_list, lg_count);
+    if constexpr (LG)
+      return tc_unit_lg(idx, B, Hq, Hkv, T, wl, wr, lg_causal, lg_list, lg_count, lg_packed,
+                        lg_tokens, lg_ntok);
     else return tc_unit(idx, B, Hq, Hkv, T, S, wl, wr);
   };
   using C = TcCfg<D>;
@@ -408,7 +432,11 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           if (!load_q(0)) break;
           const int zkv = u.b * Hkv + u.hk;
           for (int jj = 0; jj < u.cnt; ++jj) {
-            const int j = tc_tile_of<LG>(u, jj, lg_list);
+            // a packed tile of global keys (local-global) or a KV tile
+            const bool pk = LG && lg_packed && jj >= u.nband;
+            const int j = pk ? jj - u.nband : tc_tile_of<LG>(u, jj, lg_list);
+            const CUtensorMap* map_k = pk ? &tmKg : &tmK;
+            const CUtensorMap* map_v = pk ? &tmVg : &tmV;
             const int sk = kc % NSK, sv = vc % NSV;
             if (kc >= NSK && !wait_bar(&bar_kempty[sk], ((kc / NSK) - 1) & 1, abort_flag,
                                        &g_tc_err, kErrWaitLoad)) {
@@ -418,7 +446,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             ptx::mbar_arrive_expect_tx(&bar_kfull[sk], TILE);
 #pragma unroll
             for (int bx = 0; bx < Tile::NBOX; ++bx)
-              ptx::tma_load_3d_hint(sK + sk * TILE + bx * Tile::BOX_BYTES, &tmK, &bar_kfull[sk],
+              ptx::tma_load_3d_hint(sK + sk * TILE + bx * Tile::BOX_BYTES, map_k, &bar_kfull[sk],
                                     bx * 64, j * 128, zkv, pol_kv);
             ++kc;
             if (vc >= NSV && !wait_bar(&bar_vempty[sv], ((vc / NSV) - 1) & 1, abort_flag,
@@ -429,7 +457,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             ptx::mbar_arrive_expect_tx(&bar_vfull[sv], TILE);
 #pragma unroll
             for (int bx = 0; bx < Tile::NBOX; ++bx)
-              ptx::tma_load_3d_hint(sV + sv * TILE + bx * Tile::BOX_BYTES, &tmV, &bar_vfull[sv],
+              ptx::tma_load_3d_hint(sV + sv * TILE + bx * Tile::BOX_BYTES, map_v, &bar_vfull[sv],
                                     bx * 64, j * 128, zkv, pol_kv);
             ++vc;
             if (jj == 0 && !load_q(1)) {
@@ -599,6 +627,18 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
       const int grow = q_start + row;
       float m_ref = -INFINITY;
       float l = 0.f;
+      // packed global keys: this row keeps packed positions [0, pk_c) outside
+      // [pk_a, pk_b), the tokens in its band (the band tiles hold those) and,
+      // when causal, those after the row excluded
+      int pk_a = 0, pk_b = 0, pk_c = 0;
+      if constexpr (LG) {
+        if (lg_packed) {
+          const int G = __ldg(lg_ntok);
+          pk_a = wl < 0 ? 0 : tc_lower_bound(lg_tokens, G, grow - wl);
+          pk_b = wr < 0 ? G : tc_lower_bound(lg_tokens, G, grow + wr + 1);
+          pk_c = lg_causal ? tc_lower_bound(lg_tokens, G, grow + 1) : G;
+        }
+      }
 
       for (int j = js; j < je; ++j, ++it) {
         // warp-uniform decision: the tcgen05.ld/st below are warp-collective
@@ -616,16 +656,31 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         // never 0: the host passes the smallest normal float for scale = 0)
         // a tile needs the mask unless all its keys lie in every row's band
         // [row - wl, row + wr] and before T
-        const int kb = tc_tile_of<LG>(u, j, lg_list) * 128;
-        const bool inside = kb + 127 < T && (wr < 0 || kb + 127 <= q_start + wr) &&
+        const bool pk = LG && lg_packed && j >= u.nband;  // a packed tile of global keys
+        const int kb = pk ? 0 : tc_tile_of<LG>(u, j, lg_list) * 128;
+        const bool inside = !pk && kb + 127 < T && (wr < 0 || kb + 127 <= q_start + wr) &&
                             (wl < 0 || kb >= q_start + 127 - wl);
-        if (!inside) {
+        if (!inside && pk) {
+          // packed positions [0, pk_c) outside [pk_a, pk_b), one keep word
+          // per 32 columns
+          const int pb = (j - u.nband) * 128;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t keep = tc_range_bits(0, pk_c - 1 - pb, 32 * g) &
+                                  ~tc_range_bits(pk_a - pb, pk_b - 1 - pb, 32 * g);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
+          }
+        } else if (!inside) {
           const int hi_c = (wr < 0 ? T - 1 : min(T - 1, grow + wr)) - kb;  // last kept column
           const int lo_c = wl < 0 ? -1 : grow - wl - kb;                     // first kept
           if constexpr (LG) {
             // band OR a global key (before T, and not after the row when
-            // causal), as one keep word per 32 columns
-            const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(lg_bits) + (kb >> 7));
+            // causal), as one keep word per 32 columns; with packed global
+            // keys the band tiles keep their band only
+            const uint4 g4 = lg_packed ? make_uint4(0u, 0u, 0u, 0u)
+                                       : __ldg(reinterpret_cast<const uint4*>(lg_bits) + (kb >> 7));
             const int ghi_c = (lg_causal ? min(T - 1, grow) : T - 1) - kb;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
@@ -916,6 +971,17 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
   if ((r = make_tmap_16bit(&mv, a.v, D, a.T, static_cast<long long>(a.B) * a.Hkv, Tile::BOX_X,
                            Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
     return cu_status(r);
+  // packed global keys (local-global): the same boxes over [B*Hkv][rows][d];
+  // otherwise K and V stand in (never read)
+  CUtensorMap mkg = mk, mvg = mv;
+  if (a.lg_packed) {
+    if ((r = make_tmap_16bit(&mkg, a.lg_kg, D, a.lg_rows, static_cast<long long>(a.B) * a.Hkv,
+                             Tile::BOX_X, Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
+      return cu_status(r);
+    if ((r = make_tmap_16bit(&mvg, a.lg_vg, D, a.lg_rows, static_cast<long long>(a.B) * a.Hkv,
+                             Tile::BOX_X, Tile::TMA_SWIZZLE, F16)) != CUDA_SUCCESS)
+      return cu_status(r);
+  }
   const long long units = static_cast<long long>(a.B) * a.Hq * ((a.T + 255) / 256) * S;
   const long long grid = units < tc_sm_count() ? units : tc_sm_count();  // one CTA per SM
   // scale * log2(e); never exactly 0, so that masked (infinite) scores give
@@ -928,7 +994,8 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, static_cast<uint16_t*>(a.o), a.lse, a.B, a.Hq, a.Hkv, a.T, scale_log2,
       static_cast<int>(units), S, S > 1 ? part_o : nullptr, S > 1 ? part_lse : nullptr, wl, wr,
-      a.lg_bits, a.lg_list, a.lg_count, a.causal);
+      a.lg_bits, a.lg_list, a.lg_count, a.causal, mkg, mvg, a.lg_packed ? 1 : 0, a.lg_tokens,
+      a.lg_ntok);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return cuda_status(e);
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.T;

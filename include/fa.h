@@ -96,7 +96,9 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
  * one of the global tokens (torch.isin over the key index) -- global tokens are
  * keys that every query attends to.  With causal = 1 the union is intersected
  * with j <= i.  The KV tiles a query tile visits are those of its band plus
- * the tiles holding a global key; all others are skipped.
+ * the tiles holding a global key, or, with the larger workspace of
+ * fa_fwd_local_global_packed_workspace_size, its band's tiles plus the global
+ * keys gathered into packed 128-row tiles; all others are skipped.
  *   local_window  : >= 0
  *   global_tokens : DEVICE array of num_global int32 key indices, any order
  *                   (4-byte aligned; may be NULL when num_global = 0); repeats
@@ -104,9 +106,12 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
  *   workspace     : DEVICE scratch of at least
  *                   fa_fwd_local_global_workspace_size(T) bytes, 16-byte
  *                   aligned, not overlapping any other buffer; contents on
- *                   entry ignored, on return undefined
+ *                   entry ignored, on return undefined.  With at least
+ *                   fa_fwd_local_global_packed_workspace_size(...) bytes the
+ *                   global keys are packed (16-bit inputs, num_global > 0)
  * Other arguments and results as fa_fwd.  Enqueues a memset and three kernels
- * (key bitmask, list of tiles holding global keys, attention).  Errors: as
+ * (key bitmask, list of tiles holding global keys, attention), and two more
+ * when packing (the sorted token list, the gather of their K and V rows).  Errors: as
  * fa_fwd, plus FA_ERR_INVALID_ARG for local_window < 0, num_global < 0, a
  * NULL global_tokens with num_global > 0 or an overlapping workspace;
  * FA_ERR_MISALIGNED for a global_tokens pointer that is not 4-byte aligned;
@@ -121,6 +126,19 @@ fa_status fa_fwd_local_global(const void* q, const void* k, const void* v, void*
  * global keys and the list of 128-key tiles holding one: 20 bytes per tile,
  * plus 16); 0 for T <= 0. */
 unsigned long long fa_fwd_local_global_workspace_size(int T);
+
+/* Bytes of workspace with which fa_fwd_local_global packs the global keys
+ * (bf16 and fp16 inputs): fa_fwd_local_global_workspace_size(T) plus the
+ * sorted distinct tokens and their K and V rows gathered per (batch, KV head)
+ * into 128-row tiles, R * 4 + 16 + 2 * B * Hkv * R * d * 2 bytes with R =
+ * num_global rounded up to a multiple of 128 (at least 128).  A query tile
+ * then visits its band's KV tiles plus ceil(#distinct tokens / 128) packed
+ * tiles, instead of every 128-key tile that holds a global key; the results
+ * are the same.  With a smaller workspace (at least the size above) the call
+ * visits whole tiles.  For fp32 inputs, or num_global = 0, the same as
+ * fa_fwd_local_global_workspace_size(T).  0 for invalid sizes or dtype. */
+unsigned long long fa_fwd_local_global_packed_workspace_size(int B, int Hkv, int T, int d,
+                                                             fa_dtype dtype, int num_global);
 
 /* Split-KV forward (FlashDecoding-style; "Flash Attention Memory Optimization
  * Explained", section "Why It Matters", names FlashDecoding as the inference

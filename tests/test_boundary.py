@@ -275,6 +275,23 @@ def test_local_global_workspace_size(lib):
     assert fa.fa_fwd_local_global_workspace_size(0) == 0
 
 
+def test_local_global_packed_workspace_size(lib):
+    # the tile-mode bytes, then R ints (R = tokens rounded up to 128, at least
+    # 128), a 16-byte count and the packed K and V rows: 2 * B * Hkv * R * d * 2
+    lg = fa.fa_fwd_local_global_workspace_size(1000)
+    bf16, f32 = fa.FA_DTYPE_BF16, fa.FA_DTYPE_F32
+    assert (fa.fa_fwd_local_global_packed_workspace_size(2, 4, 1000, 64, bf16, 37)
+            == lg + 128 * 4 + 16 + 2 * 2 * 4 * 128 * 64 * 2)
+    assert (fa.fa_fwd_local_global_packed_workspace_size(1, 1, 1000, 128, bf16, 300)
+            == lg + 384 * 4 + 16 + 2 * 384 * 128 * 2)
+    # fp32 inputs and no tokens need no packing; invalid sizes give 0
+    assert fa.fa_fwd_local_global_packed_workspace_size(2, 4, 1000, 64, f32, 37) == lg
+    assert fa.fa_fwd_local_global_packed_workspace_size(2, 4, 1000, 64, bf16, 0) == lg
+    assert fa.fa_fwd_local_global_packed_workspace_size(0, 4, 1000, 64, bf16, 3) == 0
+    assert fa.fa_fwd_local_global_packed_workspace_size(2, 4, 1000, 64, bf16, -1) == 0
+    assert fa.fa_fwd_local_global_packed_workspace_size(2, 4, 1000, 64, 9, 3) == 0
+
+
 def test_local_global_rejects_bad_arguments_on_the_host(lib):
     assert lg_call(w=-1) == fa.FA_ERR_INVALID_ARG
     assert lg_call(n=-2) == fa.FA_ERR_INVALID_ARG

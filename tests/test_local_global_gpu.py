@@ -1,5 +1,6 @@
 """GPU parity of the local-global mask (fa_fwd_local_global) against the
-fp64 oracle, through the C ABI.
+fp64 oracle, through the C ABI, with the global keys packed into dense tiles
+(the default of the 16-bit path) and visited as whole key tiles.
 
 The yelogs.com Flash Attention2/Triton tutorial, section "1. 稀疏注意力支持",
 keeps key j for query i when |i - j| <= local_window or j is a global token
@@ -36,16 +37,24 @@ def global_set(kind, T, seed):
         # unsorted, with repeats and entries outside [0, T)
         g = rng.integers(-20, T + 20, size=37).tolist()
         return g + g[:5]
+    if kind == "dense":
+        # more than 128 distinct tokens: several packed tiles, many of them
+        # inside the rows' bands
+        return rng.permutation(T)[: min(T, 300)].tolist()
+    if kind == "near":
+        # clustered around the middle: inside the band of the middle rows,
+        # outside it for the others
+        return list(range(T // 2 - 20, T // 2 + 20, 3))
     raise ValueError(kind)
 
 
-def run_lg(fa, B, Hq, Hkv, T, d, w, kind, causal, dtype, seed):
+def run_lg(fa, B, Hq, Hkv, T, d, w, kind, causal, dtype, seed, pack=True):
     q, k, v = make_qkv(B, Hq, Hkv, T, d, dtype=dtype, seed=seed)
     g = global_set(kind, T, seed)
     gt = torch.tensor(g, dtype=torch.int32, device="cuda")
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, window=(w, w),
-                    global_tokens=gt)
+                    global_tokens=gt, pack_global=pack)
     torch.cuda.synchronize()
     assert fa.fa_debug_sync_check() == 0
     O_ref, L_ref = oracle.attention_ref(q, k, v, scale, causal, window=(w, w), global_tokens=g)
@@ -59,12 +68,31 @@ def run_lg(fa, B, Hq, Hkv, T, d, w, kind, causal, dtype, seed):
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("kind,w", [("none", 3), ("sink", 0), ("sinks4", 64), ("last", 5),
-                                    ("strided", 1), ("random", 200)])
+                                    ("strided", 1), ("random", 200), ("dense", 40),
+                                    ("near", 30)])
 @pytest.mark.parametrize("T,d", [(129, 32), (640, 128), (1000, 64), (2500, 128)])
 def test_local_global_parity(cuda_lib, T, d, kind, w, causal, dtype):
-    """Band tiles plus tiles holding a global key below, inside or above
-    the band, ragged T, repeats and out-of-range entries."""
+    """Band tiles plus global keys below, inside or above the band, ragged T,
+    repeats and out-of-range entries; the 16-bit path packs the global keys."""
     run_lg(cuda_lib, 1, 2, 1, T, d, w, kind, causal, dtype, seed=T + d + w)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("kind,w", [("sinks4", 64), ("strided", 1), ("random", 200),
+                                    ("dense", 40), ("near", 30)])
+@pytest.mark.parametrize("T,d", [(640, 128), (1000, 64)])
+def test_local_global_parity_whole_tiles(cuda_lib, T, d, kind, w, causal, dtype):
+    """The same mask with the global keys visited as whole key tiles (the
+    smaller workspace)."""
+    run_lg(cuda_lib, 1, 2, 1, T, d, w, kind, causal, dtype, seed=T + d + w, pack=False)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_local_global_packed_many_tokens_and_heads(cuda_lib, causal):
+    """Three packed tiles (300 distinct tokens), GQA heads, d = 16."""
+    run_lg(cuda_lib, 2, 4, 2, 1777, 16, 9, "dense", causal, "bf16", seed=11)
+    run_lg(cuda_lib, 2, 6, 3, 900, 128, 0, "dense", causal, "f16", seed=12)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
