@@ -304,6 +304,14 @@ def test_local_global_rejects_bad_arguments_on_the_host(lib):
     assert lg_call(gt=O + 64) == fa.FA_ERR_INVALID_ARG       # tokens overlap an output
     assert lg_call(q=0) == fa.FA_ERR_INVALID_ARG             # the fa_fwd checks apply
     assert lg_call(d=40) == fa.FA_ERR_UNSUPPORTED
+    # with the packing size the overlap check covers the packed K/V rows too:
+    # a workspace that ends 64 bytes before O in whole-tile mode reaches into
+    # O once it is large enough to pack
+    lg = fa.fa_fwd_local_global_workspace_size(GOOD["T"])
+    packed = fa.fa_fwd_local_global_packed_workspace_size(GOOD["B"], GOOD["Hkv"], GOOD["T"],
+                                                          GOOD["d"], GOOD["dtype"], 5)
+    assert packed > lg + 64
+    assert lg_call(ws=O - lg - 64, ws_bytes=packed) == fa.FA_ERR_INVALID_ARG
 
 
 def test_bwd_local_global_workspace_and_host_errors(lib):
