@@ -95,3 +95,13 @@ def test_clock_summary_flags_throttling():
     out = s.summary(10.0, 10.2)
     assert out["sm_mhz"] == 1850 and out["sm_max_mhz"] == 2070
     assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_alu_and_exp_peaks_from_unit_counts():
+    # 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz; 32 ex2 per clock per SM
+    p = bench.alu_peaks({"sm_max_mhz": 2070.0}, 152)
+    assert abs(p["fp32_tflops"] - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+    assert abs(p["fp32_tflops"] - 80.55) < 0.01
+    assert abs(p["exp_per_s"] - 152 * 32 * 2.07e9) < 1.0
+    # without a measured clock the maximum GB300 clock stands in
+    assert bench.alu_peaks({}, 152) == p
