@@ -692,9 +692,14 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
                 if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
             }
           } else {
+            // the band's columns [lo_c, hi_c] as one keep word per 32 columns
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c > hi_c || c < lo_c) s[c >> 5][c & 31] = __float_as_uint(mask_val);
+            for (int g = 0; g < 4; ++g) {
+              const uint32_t keep = tc_range_bits(lo_c, hi_c, 32 * g);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
+            }
           }
         }
         // row maximum (minimum when scale < 0) with four independent chains
