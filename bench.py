@@ -103,17 +103,88 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+PIPE_RATES_FILE = os.path.join(ROOT, "profiles", "pipe_rates_gb300.md")
+
+
+def measured_pipe_rates() -> dict:
+    """Per-SM, per-clock instruction rates of the special-function and FMA
+    pipes, from the committed record of `bench.py --measure-pipe-rates`
+    (lines `key = value`); empty if that record is absent."""
+    out = {}
+    if os.path.exists(PIPE_RATES_FILE):
+        with open(PIPE_RATES_FILE) as f:
+            for line in f:
+                line = line.strip().lstrip("- ")
+                if " = " in line:
+                    k, v = line.split(" = ", 1)
+                    try:
+                        out[k.strip()] = float(v.split()[0])
+                    except ValueError:
+                        pass
+    return out
+
+
 def alu_peaks(peaks: dict, sms: int) -> dict:
-    """Peaks of the two non-tensor pipes the forward can be bound by, derived
-    from unit counts and the maximum SM clock (``sm_max_mhz`` of the measured
-    peaks, else 2070 MHz):
-      fp32_tflops: SMs x 128 FP32 lanes x 2 flops per FMA x clock (the
-                   true-fp32 CUDA-core kernel is bound by FFMA);
-      exp_per_s:   SMs x 32 ex2 per clock (one warp instruction per 4 clocks
-                   per SMSP, measured on GB300) x clock -- one exponential per
-                   kept (row, key) pair bounds the small-d shapes."""
+    """Peaks of the two non-tensor pipes the forward can be bound by, from the
+    measured per-clock rates (`bench.py --measure-pipe-rates`, recorded in
+    profiles/pipe_rates_gb300.md) x SMs x the maximum SM clock
+    (``sm_max_mhz`` of the measured peaks, else 2070 MHz):
+      fp32_tflops: FMA instructions per clock per SM x 2 flops (the
+                   true-fp32 CUDA-core kernel is bound by FFMA); 128 lanes per
+                   SM if no record exists;
+      exp_per_s:   ex2 instructions per clock per SM -- one exponential per
+                   kept (row, key) pair bounds the small-d shapes; 32 per clock
+                   (one warp instruction per 4 clocks per SMSP) if no record."""
     hz = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
-    return {"fp32_tflops": sms * 128 * 2 * hz / 1e12, "exp_per_s": sms * 32 * hz}
+    rates = measured_pipe_rates()
+    ffma = rates.get("ffma_per_clock_per_sm", 128.0)
+    ex2 = rates.get("ex2_per_clock_per_sm", 32.0)
+    return {"fp32_tflops": sms * ffma * 2 * hz / 1e12, "exp_per_s": sms * ex2 * hz,
+            "source": "measured" if rates else "assumed"}
+
+
+def measure_pipe_rates(args) -> int:
+    """Runs the pipe-rate probe (fa_unit_pipe_rate) on one GPU and prints one
+    JSON line: instructions per clock per SM (median over the CTAs, one per
+    SM, from clock64 spans) for ex2, scalar FFMA and paired FFMA, and the
+    aggregate rate per second from CUDA events."""
+    import torch
+
+    import exact_attention_90_gb300 as fa
+
+    fa.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.zeros(512, dtype=torch.float32, device=dev)
+    cycles = torch.zeros(sms, dtype=torch.int64, device=dev)
+    iters = 1 << 14
+    out = {"metric": "pipe rates", "sms": sms, "iters": iters, "threads_per_cta": 512,
+           "chains_per_thread": 8}
+    names = {0: "ex2", 1: "ffma", 2: "ffma2"}
+    for kind, name in names.items():
+        instr_per_cta = 512 * (8 if kind < 2 else 4) * iters
+        for _ in range(2):  # warm-up
+            if fa.fa_unit_pipe_rate(kind, iters, sms, sink, cycles) != 0:
+                raise RuntimeError("fa_unit_pipe_rate failed")
+        torch.cuda.synchronize(dev)
+        per_clk, per_s = [], []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if fa.fa_unit_pipe_rate(kind, iters, sms, sink, cycles) != 0:
+                raise RuntimeError("fa_unit_pipe_rate failed")
+            e1.record()
+            torch.cuda.synchronize(dev)
+            c = cycles.cpu().tolist()
+            per_clk.append(statistics.median(instr_per_cta / x for x in c))
+            per_s.append(instr_per_cta * sms / (e0.elapsed_time(e1) / 1e3))
+        out[f"{name}_per_clock_per_sm"] = round(statistics.median(per_clk), 2)
+        out[f"{name}_per_s"] = float(f"{statistics.median(per_s):.4g}")
+    # paired FMA: each instruction is two FMAs
+    out["ffma2_fma_per_clock_per_sm"] = round(2 * out["ffma2_per_clock_per_sm"], 2)
+    print(json.dumps(out), flush=True)
+    return 0
 
 
 def kernel_source_hash() -> str:
@@ -467,8 +538,11 @@ def run_ours(args, w):
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": (f"bf16_tflops (burst) of {src}" if tensor_path else
-                                     f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x "
+                                     f"derived: {sms} SMs x FFMA per clock per SM "
+                                     f"({alu['source']}) x 2 flops x "
                                      f"{float(peaks.get('sm_max_mhz', 2070.0)):.0f} MHz"),
+                     "exp_peak_source": (f"{sms} SMs x ex2 per clock per SM ({alu['source']}, "
+                                         "profiles/pipe_rates_gb300.md) x max SM clock"),
                      "exp_frac": (None if bwd else
                                   pairs / (ms_per / 1e3) / alu["exp_per_s"]),
                      "algorithmic_flops_per_launch": flops,
@@ -572,7 +646,12 @@ def main(argv=None):
     ap.add_argument("--profile", action="store_true",
                     help="device steps only (no e2e, oracle or clock sampling): for ncu")
     ap.add_argument("--B", type=int, default=0, help="override the workload's batch size")
+    ap.add_argument("--measure-pipe-rates", action="store_true",
+                    help="measure the ex2 and FMA instruction rates per clock per SM (the "
+                         "denominators of the exp and fp32 rooflines) and exit")
     args = ap.parse_args(argv)
+    if args.measure_pipe_rates:
+        return measure_pipe_rates(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     _, _, world = dist_env()

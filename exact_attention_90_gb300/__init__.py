@@ -25,7 +25,8 @@ import os
 __all__ = [
     "FaError", "load_library", "library_path", "fwd", "fa_fwd", "fa_fwd_simt",
     "fa_status_string", "fa_version", "fa_debug_sync_check", "fa_last_cuda_error",
-    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_fwd_window", "fa_fwd_split",
+    "fa_unit_tma", "fa_unit_qk", "fa_unit_pv", "fa_unit_timeout", "fa_unit_pipe_rate",
+    "fa_fwd_window", "fa_fwd_split",
     "fa_fwd_split_static",
     "fa_fwd_split_workspace_size", "fa_fwd_split_heuristic", "fa_bwd", "fa_bwd_workspace_size",
     "fa_fwd_local_global", "fa_fwd_local_global_workspace_size",
@@ -62,6 +63,7 @@ EXPORTS = [
     ("fa_unit_qk", _I, [_P, _P, _P, _I, _P]),
     ("fa_unit_pv", _I, [_P, _P, _P, _P, _I, _I, ctypes.c_uint, ctypes.c_uint, _P]),
     ("fa_unit_timeout", _I, [ctypes.c_longlong, _P, _P]),
+    ("fa_unit_pipe_rate", _I, [_I, _I, _I, _P, _P, _P]),
     ("fa_fwd_window", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     ("fa_fwd_split", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
                           ctypes.c_ulonglong, _P]),
@@ -318,6 +320,11 @@ def fa_unit_timeout(budget_cycles, gave_up, stream=None) -> int:
     return load_library().fa_unit_timeout(int(budget_cycles), _ptr(gave_up), _stream(stream))
 
 
+def fa_unit_pipe_rate(kind, iters, blocks, sink, cycles, stream=None) -> int:
+    return load_library().fa_unit_pipe_rate(int(kind), int(iters), int(blocks), _ptr(sink),
+                                            _ptr(cycles), _stream(stream))
+
+
 # ------------------------------------------------------------------ tensor API
 def _dtype_code(t) -> int:
     import torch
@@ -377,6 +384,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
     if kernel not in ("auto", "simt"):
         raise ValueError("kernel must be 'auto' or 'simt'")
+    if num_splits is not None and int(num_splits) > 1 and (window is not None
+                                                           or global_tokens is not None):
+        # the band and local-global entry points have no KV split
+        raise ValueError("num_splits > 1 cannot be combined with window or global_tokens")
     if global_tokens is not None:
         wl, wr = (0, 0) if window is None else (int(window[0]), int(window[1]))
         if wl != wr:

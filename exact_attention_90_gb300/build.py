@@ -35,9 +35,12 @@ def nvcc() -> str:
 
 
 def _flags(extra=()):
+    # FA_NVCC_FLAGS: extra nvcc flags, e.g. -D settings of the kernels' tuning
+    # macros for a comparison build
+    env = os.environ.get("FA_NVCC_FLAGS", "").split()
     return (ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                     "--expt-relaxed-constexpr", "-I", os.path.join(PKG, "..", "include")]
-            + list(extra))
+            + env + list(extra))
 
 
 def _deps_mtime() -> float:

@@ -318,6 +318,66 @@ fa_status unit_pv_impl(const float* p, const void* pb, const void* v, float* o, 
   return cuda_status(cudaGetLastError());
 }
 
+// Pipe-rate probe: every thread runs 8 independent dependency chains of one
+// instruction kind for `iters` rounds, so that the pipe, not the latency of
+// one chain, sets the pace.  Kinds: 0 = ex2.approx.ftz.f32 on the
+// special-function unit (x <- 2^-x, which stays in [0.5, 1]); 1 = scalar fp32
+// FMA; 2 = paired fp32 FMA (fma.rn.f32x2, two FMAs per instruction).  Each
+// CTA records its clock64 span; the dynamic shared memory the launch asks
+// for keeps one CTA per SM.
+constexpr int kRateThreads = 512;
+constexpr int kRateChains = 8;
+constexpr int kRateSmem = 160 * 1024;
+
+template <int KIND>
+__global__ void __launch_bounds__(kRateThreads) unit_pipe_rate_kernel(int iters, float* sink,
+                                                                      long long* cycles) {
+  float x[kRateChains];
+#pragma unroll
+  for (int i = 0; i < kRateChains; ++i) x[i] = 0.5f + 0.01f * (threadIdx.x & 7) + 0.003f * i;
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+    if constexpr (KIND == 0) {
+#pragma unroll
+      for (int i = 0; i < kRateChains; ++i) x[i] = ptx::ex2(-x[i]);
+    } else if constexpr (KIND == 1) {
+#pragma unroll
+      for (int i = 0; i < kRateChains; ++i) x[i] = fmaf(x[i], 0.999f, 0.001f);
+    } else {
+      const uint64_t a2 = ptx::f2_pack(0.999f, 0.999f), b2 = ptx::f2_pack(0.001f, 0.001f);
+#pragma unroll
+      for (int i = 0; i < kRateChains; i += 2) {
+        const uint64_t y = ptx::fma2(ptx::f2_pack(x[i], x[i + 1]), a2, b2);
+        ptx::f2_unpack(y, x[i], x[i + 1]);
+      }
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRateChains; ++i) acc += x[i];
+  if (acc == 12345.f) sink[threadIdx.x] = acc;  // keeps the chains live
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+template <int KIND>
+fa_status unit_pipe_rate_launch(int iters, int blocks, float* sink, long long* cycles,
+                                cudaStream_t st) {
+  auto kern = unit_pipe_rate_kernel<KIND>;
+  static bool attr_done[64] = {};
+  bool* done = device_flag(attr_done);
+  if (done == nullptr || !*done) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (done != nullptr) *done = true;
+  }
+  kern<<<blocks, kRateThreads, kRateSmem, st>>>(iters, sink, cycles);
+  return cuda_status(cudaGetLastError());
+}
+
 fa_status unit_timeout_impl(long long budget, int* gave_up, cudaStream_t st) {
   unit_timeout_kernel<<<1, 128, 0, st>>>(budget, gave_up);
   return cuda_status(cudaGetLastError());
@@ -380,6 +440,21 @@ fa_status fa_unit_pv(const float* p, const void* pb, const void* v, float* o, in
     case 32: return fa::unit_pv_impl<32>(p, pb, v, o, mode, lbo, sbo, st);
     case 64: return fa::unit_pv_impl<64>(p, pb, v, o, mode, lbo, sbo, st);
     default: return fa::unit_pv_impl<128>(p, pb, v, o, mode, lbo, sbo, st);
+  }
+}
+
+fa_status fa_unit_pipe_rate(int kind, int iters, int blocks, float* sink, long long* cycles,
+                            void* stream) {
+  if (!sink || !cycles || iters < 1 || iters > (1 << 24) || blocks < 1 || blocks > 4096)
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(sink) & 3u) || (reinterpret_cast<uintptr_t>(cycles) & 7u))
+    return FA_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (kind) {
+    case 0: return fa::unit_pipe_rate_launch<0>(iters, blocks, sink, cycles, st);
+    case 1: return fa::unit_pipe_rate_launch<1>(iters, blocks, sink, cycles, st);
+    case 2: return fa::unit_pipe_rate_launch<2>(iters, blocks, sink, cycles, st);
+    default: return FA_ERR_INVALID_ARG;
   }
 }
 

@@ -177,7 +177,9 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
  * smaller num_splits, or 1, which needs no scratch).
  * Set-up: the first call on each device looks up the scratch array's device
  * address (cudaGetSymbolAddress, no allocation); make that first call before
- * any stream capture.  Every call on a device shares the one array and leaves
+ * any stream capture.  The address is cached per device together with the id
+ * of the CUDA context it belongs to; after cudaDeviceReset the next call
+ * finds a new context and looks the address up again.  Every call on a device shares the one array and leaves
  * its partial results there; no call relies on earlier contents, but calls
  * that overlap on the GPU (for example on different streams) race. */
 fa_status fa_fwd_split_static(const void* q, const void* k, const void* v, void* o, float* lse,

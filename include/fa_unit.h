@@ -62,6 +62,19 @@ fa_status fa_unit_pv(const float* p, const void* pb, const void* v, float* o, in
  * *gave_up (a device int, 4-byte aligned).  The context stays usable. */
 fa_status fa_unit_timeout(long long budget_cycles, int* gave_up, void* stream);
 
+/* Pipe-rate probe, the measured denominator of the softmax rooflines: each
+ * of `blocks` CTAs (one per SM: the launch reserves 160 KB of shared memory)
+ * runs 512 threads x 8 independent chains x `iters` rounds of one
+ * instruction kind -- 0: ex2.approx.ftz.f32 (special-function unit), 1:
+ * scalar fp32 FMA, 2: paired fp32 FMA (fma.rn.f32x2) -- and writes its
+ * clock64 span to cycles[blockIdx] (device, blocks entries, 8-byte aligned).
+ * Instructions per CTA = 512 * 8 * iters for kinds 0 and 1, 512 * 4 * iters
+ * for kind 2 (two FMAs each).  sink: device float[512], written only if the
+ * chains reach an impossible value (keeps them live).  iters 1 .. 2^24,
+ * blocks 1 .. 4096; FA_ERR_INVALID_ARG otherwise. */
+fa_status fa_unit_pipe_rate(int kind, int iters, int blocks, float* sink, long long* cycles,
+                            void* stream);
+
 /* The fp32 CUDA-core attention kernel for fp32 or bf16 inputs (same
  * arguments and semantics as fa_fwd). */
 fa_status fa_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -97,11 +97,28 @@ def test_clock_summary_flags_throttling():
     assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
 
 
-def test_alu_and_exp_peaks_from_unit_counts():
-    # 152 SMs x 128 FP32 lanes x 2 flops (FMA) x 2.07 GHz; 32 ex2 per clock per SM
+def test_alu_and_exp_peaks_from_measured_rates():
+    # SMs x rate per clock per SM x the maximum clock; the rates come from the
+    # committed record of `bench.py --measure-pipe-rates`, else the unit
+    # counts (128 FP32 lanes, 32 ex2 per clock per SM)
+    rates = bench.measured_pipe_rates()
+    ffma = rates.get("ffma_per_clock_per_sm", 128.0)
+    ex2 = rates.get("ex2_per_clock_per_sm", 32.0)
     p = bench.alu_peaks({"sm_max_mhz": 2070.0}, 152)
-    assert abs(p["fp32_tflops"] - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
-    assert abs(p["fp32_tflops"] - 80.55) < 0.01
-    assert abs(p["exp_per_s"] - 152 * 32 * 2.07e9) < 1.0
+    assert abs(p["fp32_tflops"] - 152 * ffma * 2 * 2.07e9 / 1e12) < 1e-9
+    assert abs(p["exp_per_s"] - 152 * ex2 * 2.07e9) < 1.0
+    assert p["source"] == ("measured" if rates else "assumed")
     # without a measured clock the maximum GB300 clock stands in
     assert bench.alu_peaks({}, 152) == p
+
+
+def test_pipe_rate_record_parses(tmp_path, monkeypatch):
+    f = tmp_path / "rates.md"
+    f.write_text("# rates\n\n- ex2_per_clock_per_sm = 31.9 (median)\n"
+                 "- ffma_per_clock_per_sm = 127.5\nnot a value = x\n")
+    monkeypatch.setattr(bench, "PIPE_RATES_FILE", str(f))
+    r = bench.measured_pipe_rates()
+    assert r == {"ex2_per_clock_per_sm": 31.9, "ffma_per_clock_per_sm": 127.5}
+    p = bench.alu_peaks({"sm_max_mhz": 2000.0}, 100)
+    assert abs(p["exp_per_s"] - 100 * 31.9 * 2e9) < 1.0
+    assert abs(p["fp32_tflops"] - 100 * 127.5 * 2 * 2e9 / 1e12) < 1e-9
