@@ -129,15 +129,17 @@ def alu_peaks(peaks: dict, sms: int) -> dict:
     measured per-clock rates (`bench.py --measure-pipe-rates`, recorded in
     profiles/pipe_rates_gb300.md) x SMs x the maximum SM clock
     (``sm_max_mhz`` of the measured peaks, else 2070 MHz):
-      fp32_tflops: FMA instructions per clock per SM x 2 flops (the
-                   true-fp32 CUDA-core kernel is bound by FFMA); 128 lanes per
-                   SM if no record exists;
+      fp32_tflops: FMAs per clock per SM (the larger of the scalar and
+                   paired rates) x 2 flops (the true-fp32 CUDA-core kernel is
+                   bound by FFMA); 128 lanes per SM if no record exists;
       exp_per_s:   ex2 instructions per clock per SM -- one exponential per
                    kept (row, key) pair bounds the small-d shapes; 32 per clock
                    (one warp instruction per 4 clocks per SMSP) if no record."""
     hz = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
     rates = measured_pipe_rates()
-    ffma = rates.get("ffma_per_clock_per_sm", 128.0)
+    # the FMA pipe's capacity: the larger of the scalar and paired FMA rates
+    ffma = max(rates.get("ffma_per_clock_per_sm", 0.0),
+               rates.get("ffma2_fma_per_clock_per_sm", 0.0)) or 128.0
     ex2 = rates.get("ex2_per_clock_per_sm", 32.0)
     return {"fp32_tflops": sms * ffma * 2 * hz / 1e12, "exp_per_s": sms * ex2 * hz,
             "source": "measured" if rates else "assumed"}

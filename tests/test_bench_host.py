@@ -102,7 +102,8 @@ def test_alu_and_exp_peaks_from_measured_rates():
     # committed record of `bench.py --measure-pipe-rates`, else the unit
     # counts (128 FP32 lanes, 32 ex2 per clock per SM)
     rates = bench.measured_pipe_rates()
-    ffma = rates.get("ffma_per_clock_per_sm", 128.0)
+    ffma = max(rates.get("ffma_per_clock_per_sm", 0.0),
+               rates.get("ffma2_fma_per_clock_per_sm", 0.0)) or 128.0
     ex2 = rates.get("ex2_per_clock_per_sm", 32.0)
     p = bench.alu_peaks({"sm_max_mhz": 2070.0}, 152)
     assert abs(p["fp32_tflops"] - 152 * ffma * 2 * 2.07e9 / 1e12) < 1e-9
