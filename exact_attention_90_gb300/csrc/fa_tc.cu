@@ -337,6 +337,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // a programmatic dependent of this grid (the split merge) may be scheduled
+  // from now on; it waits for this grid's completion before it reads
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     const Smem m(smem_raw);
     uint64_t *bar_qfull = m.qfull, *bar_qempty = m.qempty, *bar_kfull = m.kfull,
@@ -886,12 +889,18 @@ static int tc_sm_count() {
 //   L = m + ln sum_s exp(L_s - m),  m = max_s L_s,
 //   O = sum_s exp(L_s - L) O_s,
 // the same online-softmax rescaling, applied across splits instead of tiles.
-// Only the splits whose KV range reaches the row's tile are read.
+// Only the splits whose KV range reaches the row's tile are read.  The lanes
+// read the splits' L_s side by side (32 at a time) and each lane owns four
+// consecutive columns of O, so that the loads of all splits are independent
+// of one another: the merge costs a few memory round trips, not two per
+// split.  Launched as a programmatic dependent of the attention kernel: the
+// grid may start early and waits here until that kernel's writes are visible.
 template <bool F16>
 __global__ void __launch_bounds__(256)
     fa_split_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                             uint16_t* __restrict__ O, float* __restrict__ LSE, int BH, int T,
                             int D, int S, int wl, int wr) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long rows = static_cast<long long>(BH) * T;
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -914,34 +923,52 @@ __global__ void __launch_bounds__(256)
   // splits [ulo + sp * chunk, ...) that hold part of [rlo, rhi)
   const int sp_first = (rlo - ulo) / chunk;
   const int ns = min(S, (rhi - ulo + chunk - 1) / chunk);
+  // m = max_s L_s over the lanes' splits sp_first + lane + 32 i
   float m = -INFINITY;
-  for (int sp = sp_first; sp < ns; ++sp) m = fmaxf(m, part_lse[sp * rows + row]);
+  for (int sp = sp_first + lane; sp < ns; sp += 32) m = fmaxf(m, part_lse[sp * rows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  // four consecutive columns per lane (lanes past d re-read column 0 and
+  // store nothing); the weights of 32 splits at a time come from the lanes
+  // that read their L_s.  Eight splits' loads are issued together, so that
+  // each batch costs one memory round trip.
+  const int c4 = lane * 4;
+  const bool col_ok = c4 < D;
+  const int c4c = col_ok ? c4 : 0;
   float wsum = 0.f;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int sp = sp_first; sp < ns; ++sp) {
-    const float w = expf(part_lse[sp * rows + row] - m);
-    wsum += w;
-    const float* po = part_o + (sp * rows + row) * D;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = sp_first; base < ns; base += 32) {
+    const int mine = base + lane;
+    const float w_mine = mine < ns ? expf(part_lse[mine * rows + row] - m) : 0.f;
+    wsum += w_mine;
+    const int cnt = min(32, ns - base);
+    for (int i0 = 0; i0 < cnt; i0 += 8) {
+      float4 x[8];
+      float w[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = lane + 32 * i;
-      if (c < D) acc[i] = fmaf(w, po[c], acc[i]);
-    }
-  }
-  const float inv = 1.f / wsum;
+      for (int u = 0; u < 8; ++u) {
+        const int i = min(i0 + u, cnt - 1);  // past the last split: weight 0
+        w[u] = __shfl_sync(0xffffffffu, w_mine, i);
+        if (i0 + u >= cnt) w[u] = 0.f;
+        x[u] = __ldg(reinterpret_cast<const float4*>(part_o + ((base + i) * rows + row) * D + c4c));
+      }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int c = lane + 32 * i;
-    if (c < D) {
-      const float y = acc[i] * inv;
-      if constexpr (F16) {
-        const __half hv = __float2half_rn(y);
-        O[row * D + c] = *reinterpret_cast<const uint16_t*>(&hv);
-      } else {
-        const __nv_bfloat16 hv = __float2bfloat16_rn(y);
-        O[row * D + c] = *reinterpret_cast<const uint16_t*>(&hv);
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(w[u], x[u].x, acc.x);
+        acc.y = fmaf(w[u], x[u].y, acc.y);
+        acc.z = fmaf(w[u], x[u].z, acc.z);
+        acc.w = fmaf(w[u], x[u].w, acc.w);
       }
     }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  const float inv = 1.f / wsum;
+  if (col_ok) {
+    uint2 packed;
+    packed.x = ptx::pack_x2<F16>(acc.x * inv, acc.y * inv);
+    packed.y = ptx::pack_x2<F16>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(O + row * D + c4) = packed;
   }
   if (lane == 0) LSE[row] = m + logf(wsum);
 }
@@ -1003,10 +1030,24 @@ static fa_status launch_tc_impl(const FwdArgs& a, int S, float* part_o, float* p
       a.lg_ntok);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return cuda_status(e);
+  // the merge, as a programmatic dependent launch: its grid may be scheduled
+  // while the attention kernel finishes (every attention CTA signals that
+  // at its start) and waits inside for that kernel's writes
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.T;
-  fa_split_combine_kernel<F16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0,
-                                 a.stream>>>(part_o, part_lse, static_cast<uint16_t*>(a.o), a.lse,
-                                             a.B * a.Hq, a.T, D, S, wl, wr);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows * 32 + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fa_split_combine_kernel<F16>, static_cast<const float*>(part_o),
+                         static_cast<const float*>(part_lse), static_cast<uint16_t*>(a.o), a.lse,
+                         a.B * a.Hq, a.T, a.d, S, wl, wr);
+  if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(cudaGetLastError());
 }
 
