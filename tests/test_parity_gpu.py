@@ -158,6 +158,22 @@ def test_split_kv_parity(cuda_lib, T, d, splits, causal, dtype):
     check_full(o, lse, q, k, v, scale, causal, what=f"split={splits} T={T} d={d} {dtype}")
 
 
+def test_split_count_with_a_mask_that_has_no_split_is_refused(cuda_lib):
+    """The band and local-global paths have no KV split: asking for one with
+    them is an error, not a silently unsplit run."""
+    fa = cuda_lib
+    q, k, v = make_qkv(1, 2, 2, 300, 64, dtype="bf16", seed=5, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fwd(q, k, v, causal=True, window=(64, 0), num_splits=2)
+    g = torch.tensor([0, 5], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fwd(q, k, v, causal=True, global_tokens=g, num_splits=3)
+    # num_splits = 1 (or None) with a window is an ordinary banded call
+    o, lse = fa.fwd(q, k, v, causal=True, window=(64, 0), num_splits=1)
+    torch.cuda.synchronize()
+    assert fa.fa_debug_sync_check() == 0
+
+
 def test_split_heuristic_path_matches_unsplit(cuda_lib):
     """A shape the heuristic splits (one head of T = 4096) gives the oracle's
     result and agrees with the unsplit kernel."""
