@@ -46,7 +46,9 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
 template <>
 __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
 
-// D_i = sum_c dO[i][c] * O[i][c] and lse_i * log2(e), one warp per padded row
+// -D_i = -sum_c dO[i][c] * O[i][c] and -lse_i * log2(e), one warp per padded
+// row.  Stored negated, so that the tensor-core kernels add them with paired
+// fp32 adds and FMAs; padded rows get -D = 0 and -lse log2(e) = -inf (P = 0).
 template <typename Tin>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const Tin* __restrict__ o, const Tin* __restrict__ d_o,
@@ -65,8 +67,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
-    delta[row] = acc;
-    lse2[row] = i < T ? lse[static_cast<size_t>(bh) * T + i] * kLog2e : INFINITY;
+    delta[row] = -acc;
+    lse2[row] = i < T ? -(lse[static_cast<size_t>(bh) * T + i] * kLog2e) : -INFINITY;
   }
 }
 
@@ -223,8 +225,8 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const size_t r = static_cast<size_t>(bh) * Tp + q0 + ty * 8 + i;  // < Tp: rows are padded
-    Lr[i] = lse2[r];
-    Dr[i] = delta[r];
+    Lr[i] = -lse2[r];  // the workspace holds -lse log2(e) and -D
+    Dr[i] = -delta[r];
   }
   float acc[8][OC];
 #pragma unroll
@@ -327,8 +329,8 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const size_t r = static_cast<size_t>(bh) * Tp + q0 + tx * 4 + c;
-        Lc[c] = lse2[r];
-        Dc[c] = delta[r];
+        Lc[c] = -lse2[r];  // the workspace holds -lse log2(e) and -D
+        Dc[c] = -delta[r];
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {

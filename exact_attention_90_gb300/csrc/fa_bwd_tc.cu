@@ -6,11 +6,14 @@
 // Optimization Explained", section "Key Mechanisms", item "Backward
 // Checkpointing"):
 //   P = exp2(scale log2(e) S - lse log2(e)),  dP = dO V^T,
-//   dS = scale P (dP - D)  with  D_i = sum_c dO[i][c] O[i][c],
-//   dV = P^T dO,  dK = dS^T Q,  dQ = dS K
-// (the scale of dK and dQ is folded into dS).  D and lse log2(e) come from
-// the preparation kernel (fa_bwd_simt.cu) in a workspace whose rows are padded
-// to a multiple of 128 per head (padded rows: D = 0, lse = +inf, so P = 0).
+//   dS = P (dP - D)  with  D_i = sum_c dO[i][c] O[i][c],
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
+// (the softmax Jacobian times the scale of S; the scale is applied once to
+// the dK and dQ accumulators in the epilogues).  -D and -lse log2(e) come
+// from the preparation kernel (fa_bwd_simt.cu) in a workspace whose rows are
+// padded to a multiple of 128 per head (padded rows: -D = 0,
+// -lse log2(e) = -inf, so P = 0).  The per-element arithmetic runs on pairs
+// of fp32 values (paired FMA, add and multiply).
 //
 // Two kernels, so that no gradient is accumulated across CTAs by atomics and
 // results are deterministic (S and dP are recomputed by both):
@@ -69,6 +72,13 @@ __device__ __forceinline__ void mask_window(int window_left, int window_right, i
   constexpr bool kBand = MASK == kBwdMaskBand || MASK == kBwdMaskLocalGlobal;
   wl = kBand ? window_left : -1;
   wr = kBand ? window_right : (MASK == kBwdMaskCausal ? 0 : -1);
+}
+
+// Paired fp32 multiply (one 64-bit register pair), as ptx::fma2 / ptx::add2.
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // a bounded barrier wait by every lane of a warp, with a warp-uniform result
@@ -372,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::reg_fence(p1);
         const float* l2s = reinterpret_cast<const float*>(sStage + st * C::STAGE +
                                                           2 * TQ::TILE_BYTES);
-        const float* dls = l2s + 64;
+        const float* dls = l2s + 64;  // (l2s: -lse log2(e) per query; dls: -D)
         // the tile needs the mask unless every (key, query) pair lies in the band
         const bool inside = (wr < 0 || kb + 127 <= q0 + wr) && (wl < 0 || kb >= q0 + 63 - wl);
         int c_lo = wr < 0 ? 0 : key - wr - q0;  // first kept query column
@@ -382,6 +392,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           c_lo = lg_causal ? key - q0 : 0;
           c_hi = 63;
         }
+        // P^T = 2^(s scale log2(e) - lse log2(e)) and dS^T = P^T (dP^T - D) for two
+        // query columns at a time; the columns' -lse log2(e) and -D come from the
+        // stage as 8-byte shared loads
+        const uint64_t sl2x2 = ptx::f2_pack(scale_log2, scale_log2);
         uint32_t pp[32], dd[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -390,15 +404,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = h * 32 + e;
-            float x0 = fmaf(__uint_as_float(sv[e]), scale_log2, -l2s[c]);
-            float x1 = fmaf(__uint_as_float(sv[e + 1]), scale_log2, -l2s[c + 1]);
+            const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(l2s + c);
+            const uint64_t nd = *reinterpret_cast<const uint64_t*>(dls + c);
+            const uint64_t x2 = ptx::fma2(
+                ptx::f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl2);
+            float x0, x1;
+            ptx::f2_unpack(x2, x0, x1);
             if (!inside) {
               if (c < c_lo || c > c_hi) x0 = -INFINITY;
               if (c + 1 < c_lo || c + 1 > c_hi) x1 = -INFINITY;
             }
             const float pa = ptx::ex2(x0), pb = ptx::ex2(x1);
-            const float da = pa * (__uint_as_float(dv[e]) - dls[c]) * scale;
-            const float db = pb * (__uint_as_float(dv[e + 1]) - dls[c + 1]) * scale;
+            const uint64_t t2 = ptx::add2(
+                ptx::f2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd);
+            float da, db;
+            ptx::f2_unpack(mul2(ptx::f2_pack(pa, pb), t2), da, db);
             pp[h * 16 + e / 2] = ptx::pack_x2<F16>(pa, pb);
             dd[h * 16 + e / 2] = ptx::pack_x2<F16>(da, db);
           }
@@ -411,7 +431,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&bar_pfull[bb]);
       }
       if (!ok) break;
-      // ---- epilogue: dV and dK rows of this key (dK already carries the scale)
+      // ---- epilogue: dV and dK rows of this key (dK times the scale of S)
       ok = __all_sync(0xffffffffu,
                       wait_bar(bar_dkv, nu & 1, abort_flag, &g_bwd_err, kErrWaitEpilogue));
       ++nu;
@@ -423,6 +443,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const RowPair rp = row_pair((which == 0 ? dV : dK) + static_cast<size_t>(bhk) * T * D, D,
                                     key, T, lane);
         const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
+        const float sc = which == 0 ? 1.f : scale;
         if constexpr (D >= 32) {
 #pragma unroll
           for (int oc = 0; oc < D / 32; ++oc) {
@@ -432,7 +453,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int v = 0; v < 16; ++v)
-              pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
+              pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * sc,
+                                        __uint_as_float(o[2 * v + 1]) * sc);
             store_sector_pair(rp, oc * 32, pk);
             store_sector_pair(rp, oc * 32 + 16, pk + 8);
           }
@@ -443,7 +465,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t pk[8];
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
+            pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * sc,
+                                      __uint_as_float(o[2 * v + 1]) * sc);
           store_sector_pair(rp, 0, pk);
         }
       }
@@ -744,8 +767,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       unit_of(idx, q0, bh, lo, hi, cnt, nb, ia);
       const int q = q0 + r;
       const size_t wrow = static_cast<size_t>(bh) * Tp + q;  // q < Tp: rows are padded
-      const float l2 = lse2[wrow];
-      const float dl = delta[wrow];
+      // the row's -lse log2(e) and -D, paired for the paired fp32 arithmetic
+      const uint64_t nl2x2 = ptx::f2_pack(lse2[wrow], lse2[wrow]);
+      const uint64_t ndx2 = ptx::f2_pack(delta[wrow], delta[wrow]);
+      const uint64_t sl2x2 = ptx::f2_pack(scale_log2, scale_log2);
       for (int jj = 0; jj < cnt; ++jj, ++gs) {
         const int j = tile_of(lo, hi, nb, ia, jj);
         const int bb = gs & 1;
@@ -790,8 +815,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int c = ch * 32 + e;
-            float x0 = fmaf(__uint_as_float(s[e]), scale_log2, -l2);
-            float x1 = fmaf(__uint_as_float(s[e + 1]), scale_log2, -l2);
+            const uint64_t x2 = ptx::fma2(
+                ptx::f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2x2, nl2x2);
+            float x0, x1;
+            ptx::f2_unpack(x2, x0, x1);
             if constexpr (LG) {
               if (!((keep >> e) & 1u)) x0 = -INFINITY;
               if (!((keep >> (e + 1)) & 1u)) x1 = -INFINITY;
@@ -800,8 +827,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (c + 1 > hi_c || c + 1 < lo_c) x1 = -INFINITY;
             }
             const float pa = ptx::ex2(x0), pb = ptx::ex2(x1);
-            pk[e / 2] = ptx::pack_x2<F16>(pa * (__uint_as_float(dp[c]) - dl) * scale,
-                                          pb * (__uint_as_float(dp[c + 1]) - dl) * scale);
+            // dS = P (dP - D), two keys at a time
+            const uint64_t t2 = ptx::add2(
+                ptx::f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndx2);
+            float da, db;
+            ptx::f2_unpack(mul2(ptx::f2_pack(pa, pb), t2), da, db);
+            pk[e / 2] = ptx::pack_x2<F16>(da, db);
           }
           // dS chunk ch over columns [16 ch, 16 ch + 16), all already read
           ptx::tmem_st16(tmem + lane_off + C::COL_S + bb * 128 + ch * 16, pk);
@@ -812,7 +843,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&bar_pfull[bb]);
       }
       if (!ok) break;
-      // ---- epilogue: the dQ row (the scale is already in dS)
+      // ---- epilogue: the dQ row, times the scale of S
       ok = __all_sync(0xffffffffu,
                       wait_bar(bar_dq, nu & 1, abort_flag, &g_bwd_err, kErrWaitEpilogue));
       ++nu;
@@ -829,7 +860,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int v = 0; v < 16; ++v)
-            pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
+            pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * scale,
+                                      __uint_as_float(o[2 * v + 1]) * scale);
           store_sector_pair(rp, oc * 32, pk);
           store_sector_pair(rp, oc * 32 + 16, pk + 8);
         }
@@ -840,7 +872,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t pk[8];
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]), __uint_as_float(o[2 * v + 1]));
+          pk[v] = ptx::pack_x2<F16>(__uint_as_float(o[2 * v]) * scale,
+                                    __uint_as_float(o[2 * v + 1]) * scale);
         store_sector_pair(rp, 0, pk);
       }
       ptx::tc_fence_before();
