@@ -10,9 +10,9 @@
 //   dK = scale dS^T Q  (dK, dV summed over the query heads sharing a KV head).
 //
 // Three kernels:
-//   fa_bwd_prep_kernel      -- one warp per query row: D_i and lse_i * log2(e)
-//                              into the workspace (padded rows: 0 and +inf, so
-//                              that a padded query gets P = 0);
+//   fa_bwd_prep_kernel      -- per query row: -D_i and -lse_i * log2(e) into
+//                              the workspace (padded rows: 0 and -inf, so that
+//                              a padded query gets P = 0);
 //   fa_bwd_dq_simt_kernel   -- one CTA per 64 query rows: loops over the KV
 //                              blocks of the band, accumulates dQ in registers;
 //   fa_bwd_dkdv_simt_kernel -- one CTA per 64 keys of a KV head: loops over the
@@ -46,27 +46,49 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
 template <>
 __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
 
-// -D_i = -sum_c dO[i][c] * O[i][c] and -lse_i * log2(e), one warp per padded
-// row.  Stored negated, so that the tensor-core kernels add them with paired
-// fp32 adds and FMAs; padded rows get -D = 0 and -lse log2(e) = -inf (P = 0).
+// sum over the elements of two 16-byte vectors of products a * b
+template <typename Tin>
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b) {
+  constexpr int VEC = 16 / static_cast<int>(sizeof(Tin));
+  const Tin* x = reinterpret_cast<const Tin*>(&a);
+  const Tin* y = reinterpret_cast<const Tin*>(&b);
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc = fmaf(to_f32(x[e]), to_f32(y[e]), acc);
+  return acc;
+}
+
+// -D_i = -sum_c dO[i][c] * O[i][c] and -lse_i * log2(e) per padded row.  Stored
+// negated, so that the tensor-core kernels add them with paired fp32 adds and
+// FMAs; padded rows get -D = 0 and -lse log2(e) = -inf (P = 0).  A row is read
+// by d * sizeof(Tin) / 16 consecutive lanes (2 to 32, a power of two), one
+// 16-byte load of O and of dO each, and reduced by shuffles within that group.
 template <typename Tin>
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const Tin* __restrict__ o, const Tin* __restrict__ d_o,
                        const float* __restrict__ lse, float* __restrict__ delta,
                        float* __restrict__ lse2, long long BH, int T, int Tp, int d) {
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= BH * Tp) return;
-  const long long bh = row / Tp;
-  const int i = static_cast<int>(row - bh * Tp);
+  constexpr int VEC = 16 / static_cast<int>(sizeof(Tin));
+  const int L = d / VEC;  // lanes per row
+  const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = gtid / L;
+  const int sub = static_cast<int>(gtid - row * L);
+  const bool active = row < BH * Tp;
+  long long bh = 0;
+  int i = 0;
   float acc = 0.f;
-  if (i < T) {
-    const size_t base = (static_cast<size_t>(bh) * T + i) * d;
-    for (int c = lane; c < d; c += 32) acc = fmaf(to_f32(d_o[base + c]), to_f32(o[base + c]), acc);
+  if (active) {
+    bh = row / Tp;
+    i = static_cast<int>(row - bh * Tp);
+    if (i < T) {
+      const size_t base = (static_cast<size_t>(bh) * T + i) * d + static_cast<size_t>(sub) * VEC;
+      acc = dot16<Tin>(*reinterpret_cast<const uint4*>(o + base),
+                       *reinterpret_cast<const uint4*>(d_o + base));
+    }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+  // the row's lanes are an aligned group of L inside the warp (L divides 32)
+  for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (active && sub == 0) {
     delta[row] = -acc;
     lse2[row] = i < T ? -(lse[static_cast<size_t>(bh) * T + i] * kLog2e) : -INFINITY;
   }
@@ -363,7 +385,8 @@ fa_status launch_prep_t(const BwdArgs& a) {
   const long long BH = static_cast<long long>(a.B) * a.Hq;
   const int Tp = bwd_rows_padded(a.T);
   const long long rows = BH * Tp;
-  fa_bwd_prep_kernel<Tin><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, a.stream>>>(
+  const long long lanes = rows * (a.d * static_cast<long long>(sizeof(Tin)) / 16);
+  fa_bwd_prep_kernel<Tin><<<static_cast<unsigned>((lanes + 255) / 256), 256, 0, a.stream>>>(
       static_cast<const Tin*>(a.o), static_cast<const Tin*>(a.d_o), a.lse, a.ws_delta, a.ws_lse2,
       BH, a.T, Tp, a.d);
   return cuda_status(cudaGetLastError());
