@@ -126,6 +126,16 @@ def test_unit_entry_points_reject_bad_arguments(lib):
     assert fa.fa_unit_timeout(0, O, stream=0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_unit_timeout(1 << 40, O, stream=0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_unit_timeout(1000, O + 2, stream=0) == fa.FA_ERR_MISALIGNED
+    # the pipe-rate probe: kind 0..2, iterations 1..2^24, blocks 1..4096, both pointers
+    assert fa.fa_unit_pipe_rate(0, 16, 152, 0, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(0, 16, 152, O, 0, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(3, 16, 152, O, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(0, 0, 152, O, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(0, (1 << 24) + 1, 152, O, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(0, 16, 0, O, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(0, 16, 4097, O, O, stream=0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_unit_pipe_rate(0, 16, 152, O + 2, O, stream=0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_unit_pipe_rate(0, 16, 152, O, O + 4, stream=0) == fa.FA_ERR_MISALIGNED
 
 
 def test_tensor_api_refuses_cpu_tensors():

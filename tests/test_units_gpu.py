@@ -137,3 +137,28 @@ def test_bounded_wait_gives_up_and_reports(cuda_lib):
     torch.cuda.synchronize()
     assert fa.fa_debug_sync_check() == 0
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+def test_pipe_rate_probe_measures_plausible_rates(cuda_lib):
+    """The probe behind the exp and fp32 rooflines: one CTA per SM, every CTA
+    reports a clock span, and the rates per clock per SM lie inside what the
+    units can deliver (at most 32 lanes x 4 SMSPs per clock; ex2 on the
+    special-function unit well below the FMA rate)."""
+    fa = cuda_lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.zeros(512, dtype=torch.float32, device="cuda")
+    cycles = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    iters = 1 << 10
+    rates = {}
+    for kind, per_thread in ((0, 8), (1, 8), (2, 4)):
+        for _ in range(2):
+            assert fa.fa_unit_pipe_rate(kind, iters, sms, sink, cycles) == 0
+        torch.cuda.synchronize()
+        c = cycles.cpu()
+        assert bool((c > 0).all())
+        rates[kind] = float((512 * per_thread * iters / c.double()).median())
+    assert fa.fa_debug_sync_check() == 0
+    assert 4.0 <= rates[0] <= 64.0            # ex2 instructions per clock per SM
+    assert 32.0 <= rates[1] <= 128.0          # scalar FMA instructions
+    assert 16.0 <= rates[2] <= 64.0           # paired FMA instructions (two FMAs each)
+    assert rates[0] < rates[1]
