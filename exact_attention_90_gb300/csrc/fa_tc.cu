@@ -736,13 +736,16 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
 
         // P = 2^(s * scale_log2 - m) for two keys at a time (paired FMA),
         // rounded to bf16 pairs into the first 64 columns of S; l sums the
-        // unrounded values
+        // unrounded values.  At d = 128 the first 32 columns of P go to
+        // tensor memory while the second half is still being computed, so
+        // that only half of the store is left after the last exponential.
         const uint64_t sl2x2 = ptx::f2_pack(scale_log2, scale_log2);
         const uint64_t nmox2 = ptx::f2_pack(-mo, -mo);
         uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
         uint32_t pall[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          if (D == 128 && c == 2) ptx::tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pall[0]));
           uint32_t(&pk)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pall[16 * c]);
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
@@ -756,7 +759,10 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             pk[v] = ptx::pack_x2<F16>(p0, p1);
           }
         }
-        ptx::tmem_st64(tS, pall);
+        if constexpr (D == 128)
+          ptx::tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pall[32]));
+        else
+          ptx::tmem_st64(tS, pall);
         // O correction (lazy, warp-uniform), before P is released: the next
         // P.V MMA accumulates into O
         if (j > js && __any_sync(0xffffffffu, resc)) {
