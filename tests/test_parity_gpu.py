@@ -81,7 +81,7 @@ def fp32_lse_bound(q, k, scale):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 def test_full_parity_growing_row_max(cuda_lib, d, dtype):
     """Row maxima that keep rising along the keys: the accumulator has to be
     rescaled many times (exercises the lazy rescale of the bf16 kernel).
