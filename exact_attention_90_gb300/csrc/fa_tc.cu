@@ -32,7 +32,7 @@
 //   MMAs and commits)
 //   warp 11 completes the third warpgroup, whose registers setmaxnreg hands
 //   to the two softmax warpgroups
-// Tensor memory (512 columns x 128 lanes x 32 bit):
+// Tensor memory (512 columns x 128 lanes x 32 bit), d = 128:
 //   S0 [0,128)  S1 [128,256)  fp32 scores of Q0 K_j^T, Q1 K_j^T
 //   P0, P1      bf16 probabilities packed two per column in the first 64
 //               columns of S0 / S1 (written by the softmax warps)
@@ -44,6 +44,15 @@
 // commits overlap the other's MMAs.  S_{t,j+1} overwrites the columns of
 // P_{t,j}; it is issued after PV_{t,j} by the same thread (the issuer's
 // elected lane), and tcgen05 MMAs of one thread execute in issue order.
+// d <= 64 (SEP_P): the O accumulators take 2 x 64 columns, so P gets its own:
+//   S0 [0,128)  S1 [128,256)  O0 [256,256+d)  O1 [320,320+d)
+//   P0 [384,448)  P1 [448,512)
+// and a tile's chain loses its MMA group: the softmax signals that it has
+// read S_{t,j} (an S-read barrier), its issuer then computes S_{t,j+1} while
+// the softmax is still exponentiating, and PV_{t,j} follows once P_{t,j} is
+// stored.  The softmax stores P_{t,j} only after PV_{t,j-1} is done (the
+// P.V-done barrier), which also orders its O correction.  The two issuers
+// run without the turn word: their tiles share no tensor-memory columns.
 // The softmax works in the log2 domain (scores times scale*log2(e), exp2 on
 // the SFU) and rescales O lazily: the reference maximum is only raised when a
 // row's maximum grows by more than 2^8, so most tiles skip the O correction;
@@ -101,9 +110,17 @@ struct TcCfg : TcTile<D> {
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   // the 512 bytes after the tiles: the barriers, the TMEM address, the abort
   // flag and the issue-turn word
-  static_assert((2 * NQ + 2 * NSK + 2 * NSV + 7) * 8 + 3 * 4 <= 512, "barrier area exceeded");
+  static_assert((2 * NQ + 2 * NSK + 2 * NSV + 9) * 8 + 3 * 4 <= 512, "barrier area exceeded");
   static constexpr uint32_t TMEM_COLS = 512;
+  // SEP_P (d <= 64): P of tile t has its own 64 columns at COL_P0 + 64 t
+  // instead of the first 64 columns of S_t, so that S_t(j+1) may be issued
+  // as soon as the softmax has read S_t(j); at d = 128 the O accumulators
+  // take those columns and P overwrites S.
+  static constexpr bool SEP_P = D <= 64;
   static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
+  static constexpr uint32_t O_STRIDE = SEP_P ? 64 : 128;  // O_t at COL_O0 + O_STRIDE t
+  static constexpr uint32_t COL_P0 = SEP_P ? 384 : COL_S0;
+  static constexpr uint32_t P_STRIDE = SEP_P ? 64 : 128;  // P_t at COL_P0 + P_STRIDE t
 };
 
 // log2 headroom of the lazy rescale: P values stay below 2^8
@@ -307,7 +324,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
   // it (ptxas spills them), while these few integer operations are free.
   struct Smem {
     uint8_t *sQ, *sK, *sV;
-    uint64_t *qfull, *qempty, *kfull, *vfull, *kempty, *vempty, *sfull, *pfull, *odone, *final_;
+    uint64_t *qfull, *qempty, *kfull, *vfull, *kempty, *vempty, *sfull, *pfull, *odone, *sread,
+        *final_;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     volatile int* turn;  // MMA issue turn of the two issuing threads
@@ -326,8 +344,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
       vempty = kempty + NSK;    // V stage free: both issuers are past its P.V MMAs
       sfull = vempty + NSV;     // [2]
       pfull = sfull + 2;        // [2]
-      odone = pfull + 2;        // [2]
-      final_ = odone + 2;
+      odone = pfull + 2;        // [2] the tile's last P.V done (SEP_P: every P.V)
+      sread = odone + 2;        // [2] SEP_P: the softmax has read the tile's S
+      final_ = sread + 2;
       tmem_slot = reinterpret_cast<uint32_t*>(final_ + 1);
       abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
       turn = abort_flag + 1;
@@ -364,6 +383,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
       ptx::mbar_init(&bar_sfull[t], 1);
       ptx::mbar_init(&bar_pfull[t], 4);  // one elected lane per softmax warp
       ptx::mbar_init(&bar_odone[t], 1);
+      ptx::mbar_init(&m.sread[t], 4);  // one elected lane per softmax warp
     }
     ptx::mbar_init(bar_final, 2);
     *abort_flag = 0;
@@ -523,6 +543,87 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           *turn = 2 * ng + t + 1;
           ++ng;
         };
+        if constexpr (C::SEP_P) {
+        // Separate P columns: this thread issues S_t(j+1) as soon as the
+        // softmax has read S_t(j) and P.V_t(j) once P_t(j) is ready, without
+        // a turn; the other tile's thread does the same for its tile.  Its
+        // own MMAs execute in issue order, and the two tiles share no
+        // tensor-memory columns.
+        int sc = 0;  // S tiles issued (phases of this tile's S-read barrier)
+        for (int k = 0; ok; ++k) {
+          const int idx = tc_unit_index(k);
+          if (idx >= num_units) break;
+          const TcUnit u = unit_at(idx);
+          if (u.cnt == 0) continue;
+          const int sq = (2 * nu + t) % C::NQ;
+          if (!tc_wait_all(&bar_qfull[sq], ((2 * nu + t) / C::NQ) & 1, abort_flag, &g_tc_err,
+                        kErrWaitMma))
+            break;
+          ++nu;
+          const uint32_t qlo = Tile::kmajor_lo(aQ + sq * TILE);
+          ptx::tc_fence_after();
+          const int js = t == 0 ? u.s0 : u.s1;
+          const int je = t == 0 ? u.e0 : u.e1;
+          for (int j = -1; ok && j < u.cnt; ++j) {
+            const bool pv = j >= 0 && j >= js && j < je;
+            const bool sn = j + 1 < u.cnt && j + 1 >= js && j + 1 < je;
+            const int cv = vc + j, ck = kc + j + 1;
+            if (j + 1 < u.cnt) {
+              // both threads wait for every load before releasing its stage
+              if (!tc_wait_all(&bar_kfull[ck % NSK], (ck / NSK) & 1, abort_flag, &g_tc_err,
+                               kErrWaitMma)) {
+                ok = false;
+                break;
+              }
+              if (sn) {
+                if (sc > 0 && !tc_wait_all(&m.sread[t], (sc - 1) & 1, abort_flag, &g_tc_err,
+                                           kErrWaitMma)) {
+                  ok = false;
+                  break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t klo = Tile::kmajor_lo(aK + (ck % NSK) * TILE);
+#pragma unroll
+                for (int kk = 0; kk < Tile::QK_KSTEPS; ++kk)
+                  ptx::mma_ss_lh_e(tmem + C::COL_S0 + t * 128, qlo + Tile::kmajor_step(kk),
+                                   Tile::DESC_HI, klo + Tile::kmajor_step(kk), Tile::DESC_HI,
+                                   IDESC_QK, kk > 0 ? 1u : 0u);
+                ptx::mma_commit_e(&bar_sfull[t]);
+                ++sc;
+              }
+              ptx::mma_commit_e(&bar_kempty[ck % NSK]);
+            }
+            // Q is free once this thread's last S of the unit is issued
+            if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit_e(&bar_qempty[sq]);
+            if (j >= 0) {
+              if (!tc_wait_all(&bar_vfull[cv % NSV], (cv / NSV) & 1, abort_flag, &g_tc_err,
+                               kErrWaitMma)) {
+                ok = false;
+                break;
+              }
+              if (pv) {
+                if (!tc_wait_all(&bar_pfull[t], pc & 1, abort_flag, &g_tc_err, kErrWaitMma)) {
+                  ok = false;
+                  break;
+                }
+                ++pc;
+                ptx::tc_fence_after();
+                const uint32_t vlo = Tile::mnmajor_lo(aV + (cv % NSV) * TILE);
+#pragma unroll
+                for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
+                  ptx::mma_ts_lh_e(tmem + C::COL_O0 + t * C::O_STRIDE,
+                                   tmem + C::COL_P0 + t * C::P_STRIDE + kk * 8,
+                                   vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
+                                   (j > js || kk > 0) ? 1u : 0u);
+                ptx::mma_commit_e(&bar_odone[t]);  // P_t and O_t free again
+              }
+              ptx::mma_commit_e(&bar_vempty[cv % NSV]);
+            }
+          }
+          kc += u.cnt;
+          vc += u.cnt;
+        }
+        } else {
         for (int k = 0; ok; ++k) {
           const int idx = tc_unit_index(k);
           if (idx >= num_units) break;
@@ -571,7 +672,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
               const uint32_t vlo = Tile::mnmajor_lo(aV + (cv % NSV) * TILE);
 #pragma unroll
               for (int kk = 0; kk < Tile::PV_KSTEPS; ++kk)
-                ptx::mma_ts_lh_e(tmem + C::COL_O0 + t * 128, tmem + C::COL_S0 + t * 128 + kk * 8,
+                ptx::mma_ts_lh_e(tmem + C::COL_O0 + t * C::O_STRIDE,
+                                 tmem + C::COL_S0 + t * 128 + kk * 8,
                                vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
                                (j > js || kk > 0) ? 1u : 0u);
             }
@@ -594,6 +696,7 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           kc += u.cnt;
           vc += u.cnt;
         }
+        }
         ptx::mma_commit_e(bar_final);
         drain_bar(bar_final, 0, &g_tc_err);
       }
@@ -612,7 +715,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
     const int row = qr * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qr * 32) << 16;
     const uint32_t tS = tmem + C::COL_S0 + t * 128 + lane_off;
-    const uint32_t tO = tmem + C::COL_O0 + t * 128 + lane_off;
+    const uint32_t tO = tmem + C::COL_O0 + t * C::O_STRIDE + lane_off;
+    const uint32_t tP = tmem + C::COL_P0 + t * C::P_STRIDE + lane_off;
+    int pw = 0;  // SEP_P: P.V completions of this tile waited for
     const bool neg = scale_log2 < 0.f;
     const float mask_val = neg ? INFINITY : -INFINITY;
     int it = 0;  // S tiles of this Q tile processed so far (barrier phases)
@@ -653,6 +758,12 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         ptx::tmem_ld128(tS, sflat);
         ptx::tmem_ld_wait(sflat);
         uint32_t(&s)[4][32] = *reinterpret_cast<uint32_t(*)[4][32]>(&sflat);
+        if constexpr (C::SEP_P) {
+          // S_t(j) is in registers: the issuer may compute S_t(j+1) into it
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&m.sread[t]);
+        }
 
         // masked scores become -inf (+inf when scale < 0), so that their
         // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
@@ -759,10 +870,21 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             pk[v] = ptx::pack_x2<F16>(p0, p1);
           }
         }
-        if constexpr (D == 128)
+        if constexpr (C::SEP_P) {
+          // P_t and O_t are free once P.V_t(j-1) is done (the unit's first
+          // tile: the epilogue of the previous unit waited for its last)
+          if (j > js) {
+            ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (pw++) & 1, abort_flag,
+                                                  &g_tc_err, kErrWaitSoftmax));
+            if (!ok) break;
+            ptx::tc_fence_after();
+          }
+          ptx::tmem_st64(tP, pall);
+        } else if constexpr (D == 128) {
           ptx::tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pall[32]));
-        else
+        } else {
           ptx::tmem_st64(tS, pall);
+        }
         // O correction (lazy, warp-uniform), before P is released: the next
         // P.V MMA accumulates into O
         if (j > js && __any_sync(0xffffffffu, resc)) {
@@ -801,7 +923,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
 
       // ---- epilogue: O = O / l in bf16, L = m + ln l (the tensor core meanwhile
       // computes the next unit's first S tiles)
-      ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (ne++) & 1, abort_flag, &g_tc_err,
+      ok = __all_sync(0xffffffffu, wait_bar(&bar_odone[t], (C::SEP_P ? pw++ : ne++) & 1,
+                                            abort_flag, &g_tc_err,
                                             kErrWaitEpilogue));
       if (!ok) break;
       ptx::tc_fence_after();
