@@ -308,8 +308,9 @@ def time_oracle(w, budget_s: float):
             break
     per_head = 4.0 * w.T * w.T * w.d / (2 if w.causal else 1)
     value = heads * per_head / t_total / 1e12
-    sample = (f"{heads} whole head(s) of T={w.T} d={w.d} {w.dtype} "
-              f"{'causal' if w.causal else 'non-causal'} (1 of {w.B * w.Hq} heads each), "
+    sample = (f"the oracle on one (b, h) head of the workload (T={w.T} d={w.d} {w.dtype} "
+              f"{'causal' if w.causal else 'non-causal'}; the workload has {w.B * w.Hq} heads), "
+              f"run {heads} time(s): {heads}/{w.B * w.Hq} of the workload's work in "
               f"{t_total:.1f} s")
     return value, sample, t_total
 
