@@ -454,38 +454,54 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           };
           if (!load_q(0)) break;
           const int zkv = u.b * Hkv + u.hk;
-          for (int jj = 0; jj < u.cnt; ++jj) {
-            // a packed tile of global keys (local-global) or a KV tile
+          // KV tile of the unit's jj-th visited tile: a packed tile of global
+          // keys (local-global) or a KV tile
+          auto load_k = [&](int jj) -> bool {
             const bool pk = LG && lg_packed && jj >= u.nband;
             const int j = pk ? jj - u.nband : tc_tile_of<LG>(u, jj, lg_list);
-            const CUtensorMap* map_k = pk ? &tmKg : &tmK;
-            const CUtensorMap* map_v = pk ? &tmVg : &tmV;
-            const int sk = kc % NSK, sv = vc % NSV;
+            const int sk = kc % NSK;
             if (kc >= NSK && !wait_bar(&bar_kempty[sk], ((kc / NSK) - 1) & 1, abort_flag,
-                                       &g_tc_err, kErrWaitLoad)) {
-              ok = false;
-              break;
-            }
+                                       &g_tc_err, kErrWaitLoad))
+              return false;
             ptx::mbar_arrive_expect_tx(&bar_kfull[sk], TILE);
 #pragma unroll
             for (int bx = 0; bx < Tile::NBOX; ++bx)
-              ptx::tma_load_3d_hint(sK + sk * TILE + bx * Tile::BOX_BYTES, map_k, &bar_kfull[sk],
-                                    bx * 64, j * 128, zkv, pol_kv);
+              ptx::tma_load_3d_hint(sK + sk * TILE + bx * Tile::BOX_BYTES, pk ? &tmKg : &tmK,
+                                    &bar_kfull[sk], bx * 64, j * 128, zkv, pol_kv);
             ++kc;
+            return true;
+          };
+          auto load_v = [&](int jj) -> bool {
+            const bool pk = LG && lg_packed && jj >= u.nband;
+            const int j = pk ? jj - u.nband : tc_tile_of<LG>(u, jj, lg_list);
+            const int sv = vc % NSV;
             if (vc >= NSV && !wait_bar(&bar_vempty[sv], ((vc / NSV) - 1) & 1, abort_flag,
-                                       &g_tc_err, kErrWaitLoad)) {
-              ok = false;
-              break;
-            }
+                                       &g_tc_err, kErrWaitLoad))
+              return false;
             ptx::mbar_arrive_expect_tx(&bar_vfull[sv], TILE);
 #pragma unroll
             for (int bx = 0; bx < Tile::NBOX; ++bx)
-              ptx::tma_load_3d_hint(sV + sv * TILE + bx * Tile::BOX_BYTES, map_v, &bar_vfull[sv],
-                                    bx * 64, j * 128, zkv, pol_kv);
+              ptx::tma_load_3d_hint(sV + sv * TILE + bx * Tile::BOX_BYTES, pk ? &tmVg : &tmV,
+                                    &bar_vfull[sv], bx * 64, j * 128, zkv, pol_kv);
             ++vc;
-            if (jj == 0 && !load_q(1)) {
-              ok = false;
-              break;
+            return true;
+          };
+          if constexpr (C::SEP_P) {
+            // the issuers need K_{j+1} (the next S) before V_j (this P.V):
+            // K runs one tile ahead of V
+            for (int jj = 0; jj <= u.cnt; ++jj) {
+              if ((jj < u.cnt && !load_k(jj)) || (jj == 0 && !load_q(1)) ||
+                  (jj >= 1 && !load_v(jj - 1))) {
+                ok = false;
+                break;
+              }
+            }
+          } else {
+            for (int jj = 0; jj < u.cnt; ++jj) {
+              if (!load_k(jj) || !load_v(jj) || (jj == 0 && !load_q(1))) {
+                ok = false;
+                break;
+              }
             }
           }
         }
