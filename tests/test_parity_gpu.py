@@ -51,6 +51,20 @@ def test_full_parity_grouped_heads(cuda_lib, Hq, Hkv, dtype):
         check_full(o, lse, q, k, v, 0.125, causal, what=f"Hq={Hq} Hkv={Hkv} {dtype}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", DS)
+def test_full_parity_many_units_per_cta(cuda_lib, d, dtype):
+    """More work units than SMs (8 x 32 heads x 2 row blocks = 512 units), so
+    every CTA of the persistent grid runs several units and the barrier phase
+    counters carry across unit boundaries (including units whose second Q
+    tile is empty: T = 300); every row against the oracle."""
+    for causal in (False, True):
+        q, k, v = make_qkv(8, 32, 8, 300, d, dtype=dtype, seed=600 + d, device="cuda")
+        scale = 1.0 / math.sqrt(d)
+        o, lse = run(cuda_lib, q, k, v, causal, scale)
+        check_full(o, lse, q, k, v, scale, causal, what=f"many units d={d} {dtype}")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("scale", [0.0, -0.09, 0.7])
 def test_full_parity_scale_edge_cases(cuda_lib, scale, dtype):
