@@ -56,7 +56,11 @@
 // The softmax works in the log2 domain (scores times scale*log2(e), exp2 on
 // the SFU) and rescales O lazily: the reference maximum is only raised when a
 // row's maximum grows by more than 2^8, so most tiles skip the O correction;
-// the result is exact because O and l always share the same reference.
+// the result is exact because O and l always share the same reference.  At
+// d <= 32 and d = 128 a tile after the row's first is exponentiated against
+// the reference without its row maximum at all; the maximum, the rescale and
+// the exponentials run again only when the tile's P sum reaches 2^15 (so no P
+// can overflow fp16).
 #include <cmath>
 #include <cstdio>
 
@@ -121,6 +125,14 @@ struct TcCfg : TcTile<D> {
   static constexpr uint32_t O_STRIDE = SEP_P ? 64 : 128;  // O_t at COL_O0 + O_STRIDE t
   static constexpr uint32_t COL_P0 = SEP_P ? 384 : COL_S0;
   static constexpr uint32_t P_STRIDE = SEP_P ? 64 : 128;  // P_t at COL_P0 + P_STRIDE t
+  // SPEC_EXP (d <= 32 and d = 128): exponentials against the running
+  // reference without the row maximum (see the softmax).  A redo reads S
+  // again from tensor memory, so S must stay there until the decision: at
+  // d <= 32 the S-read signal waits for the exponentials, at d = 128 the
+  // first half of P is stored early only on the redo path.  At d = 64 the
+  // later S-read signal delays the next S (four MMA k-steps) by more than
+  // the maximum saves.
+  static constexpr bool SPEC_EXP = (SEP_P && D <= 32) || D == 128;
 };
 
 // log2 headroom of the lazy rescale: P values stay below 2^8
@@ -771,121 +783,158 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t sflat[128];
-        ptx::tmem_ld128(tS, sflat);
-        ptx::tmem_ld_wait(sflat);
         uint32_t(&s)[4][32] = *reinterpret_cast<uint32_t(*)[4][32]>(&sflat);
-        if constexpr (C::SEP_P) {
-          // S_t(j) is in registers: the issuer may compute S_t(j+1) into it
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&m.sread[t]);
-        }
+        // S of the tile into registers, masked
+        auto load_s = [&]() {
+          ptx::tmem_ld128(tS, sflat);
+          ptx::tmem_ld_wait(sflat);
 
-        // masked scores become -inf (+inf when scale < 0), so that their
-        // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
-        // never 0: the host passes the smallest normal float for scale = 0)
-        // a tile needs the mask unless all its keys lie in every row's band
-        // [row - wl, row + wr] and before T
-        const bool pk = LG && lg_packed && j >= u.nband;  // a packed tile of global keys
-        const int kb = pk ? 0 : tc_tile_of<LG>(u, j, lg_list) * 128;
-        const bool inside = !pk && kb + 127 < T && (wr < 0 || kb + 127 <= q_start + wr) &&
-                            (wl < 0 || kb >= q_start + 127 - wl);
-        if (!inside && pk) {
-          // packed positions [0, pk_c) outside [pk_a, pk_b), one keep word
-          // per 32 columns
-          const int pb = (j - u.nband) * 128;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t keep = tc_range_bits(0, pk_c - 1 - pb, 32 * g) &
-                                  ~tc_range_bits(pk_a - pb, pk_b - 1 - pb, 32 * g);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
-          }
-        } else if (!inside) {
-          const int hi_c = (wr < 0 ? T - 1 : min(T - 1, grow + wr)) - kb;  // last kept column
-          const int lo_c = wl < 0 ? -1 : grow - wl - kb;                     // first kept
-          if constexpr (LG) {
-            // band OR a global key (before T, and not after the row when
-            // causal), as one keep word per 32 columns; with packed global
-            // keys the band tiles keep their band only
-            const uint4 g4 = lg_packed ? make_uint4(0u, 0u, 0u, 0u)
-                                       : __ldg(reinterpret_cast<const uint4*>(lg_bits) + (kb >> 7));
-            const int ghi_c = (lg_causal ? min(T - 1, grow) : T - 1) - kb;
+          // masked scores become -inf (+inf when scale < 0), so that their
+          // scaled exponent is -inf and exp2 gives exactly 0 (scale_log2 is
+          // never 0: the host passes the smallest normal float for scale = 0)
+          // a tile needs the mask unless all its keys lie in every row's band
+          // [row - wl, row + wr] and before T
+          const bool pk = LG && lg_packed && j >= u.nband;  // a packed tile of global keys
+          const int kb = pk ? 0 : tc_tile_of<LG>(u, j, lg_list) * 128;
+          const bool inside = !pk && kb + 127 < T && (wr < 0 || kb + 127 <= q_start + wr) &&
+                              (wl < 0 || kb >= q_start + 127 - wl);
+          if (!inside && pk) {
+            // packed positions [0, pk_c) outside [pk_a, pk_b), one keep word
+            // per 32 columns
+            const int pb = (j - u.nband) * 128;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              const uint32_t gw = g == 0 ? g4.x : (g == 1 ? g4.y : (g == 2 ? g4.z : g4.w));
-              const uint32_t keep = tc_range_bits(lo_c, hi_c, 32 * g) |
-                                    (gw & tc_range_bits(0, ghi_c, 32 * g));
+              const uint32_t keep = tc_range_bits(0, pk_c - 1 - pb, 32 * g) &
+                                    ~tc_range_bits(pk_a - pb, pk_b - 1 - pb, 32 * g);
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
             }
-          } else {
-            // the band's columns [lo_c, hi_c] as one keep word per 32 columns
+          } else if (!inside) {
+            const int hi_c = (wr < 0 ? T - 1 : min(T - 1, grow + wr)) - kb;  // last kept column
+            const int lo_c = wl < 0 ? -1 : grow - wl - kb;                     // first kept
+            if constexpr (LG) {
+              // band OR a global key (before T, and not after the row when
+              // causal), as one keep word per 32 columns; with packed global
+              // keys the band tiles keep their band only
+              const uint4 g4 = lg_packed ? make_uint4(0u, 0u, 0u, 0u)
+                                         : __ldg(reinterpret_cast<const uint4*>(lg_bits) +
+                                                 (kb >> 7));
+              const int ghi_c = (lg_causal ? min(T - 1, grow) : T - 1) - kb;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const uint32_t keep = tc_range_bits(lo_c, hi_c, 32 * g);
+              for (int g = 0; g < 4; ++g) {
+                const uint32_t gw = g == 0 ? g4.x : (g == 1 ? g4.y : (g == 2 ? g4.z : g4.w));
+                const uint32_t keep = tc_range_bits(lo_c, hi_c, 32 * g) |
+                                      (gw & tc_range_bits(0, ghi_c, 32 * g));
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
+                for (int e = 0; e < 32; ++e)
+                  if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
+              }
+            } else {
+              // the band's columns [lo_c, hi_c] as one keep word per 32 columns
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const uint32_t keep = tc_range_bits(lo_c, hi_c, 32 * g);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (!((keep >> e) & 1u)) s[g][e] = __float_as_uint(mask_val);
+              }
             }
           }
-        }
-        // row maximum (minimum when scale < 0) with four independent chains
-        float a[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          a[c] = __uint_as_float(s[c][0]);
-#pragma unroll
-          for (int v = 1; v < 31; v += 2) {
-            const float x = __uint_as_float(s[c][v]), y = __uint_as_float(s[c][v + 1]);
-            a[c] = neg ? ptx::min3(a[c], x, y) : ptx::max3(a[c], x, y);
+        };
+        load_s();
+        auto signal_s_read = [&]() {
+          if constexpr (C::SEP_P) {
+            // S_t(j) is no longer needed: the issuer may compute S_t(j+1) into it
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&m.sread[t]);
           }
-        }
-        float mx;
-        if (!neg)
-          mx = ptx::max3(ptx::max3(a[0], a[1], __uint_as_float(s[0][31])),
-                         ptx::max3(a[2], a[3], __uint_as_float(s[1][31])),
-                         fmaxf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31])));
-        else
-          mx = ptx::min3(ptx::min3(a[0], a[1], __uint_as_float(s[0][31])),
-                         ptx::min3(a[2], a[3], __uint_as_float(s[1][31])),
-                         fminf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31])));
-        const float m_cand = mx * scale_log2;
-        const bool resc = m_cand > m_ref + FA_RESCALE_THRESHOLD;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ptx::ex2(m_ref - m_cand);  // 0 on the first tile (m_ref = -inf)
-          m_ref = m_cand;
-        }
-        const float mo = (m_ref == -INFINITY) ? 0.f : m_ref;
-
+        };
+        if constexpr (!C::SPEC_EXP) signal_s_read();
         // P = 2^(s * scale_log2 - m) for two keys at a time (paired FMA),
-        // rounded to bf16 pairs into the first 64 columns of S; l sums the
-        // unrounded values.  At d = 128 the first 32 columns of P go to
-        // tensor memory while the second half is still being computed, so
-        // that only half of the store is left after the last exponential.
+        // rounded to bf16 pairs into the first 64 columns of S (d <= 64: into
+        // P's own columns); l sums the unrounded values.  At d = 128 the first
+        // 32 columns of P go to tensor memory while the second half is still
+        // being computed, so that only half of the store is left after the
+        // last exponential.
         const uint64_t sl2x2 = ptx::f2_pack(scale_log2, scale_log2);
-        const uint64_t nmox2 = ptx::f2_pack(-mo, -mo);
-        uint64_t acc2[2] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f)};
+        uint64_t acc2[2];
         uint32_t pall[64];
+        bool early = false;  // d = 128: the first half of P already stored
+        auto exps = [&](float mo, bool allow_early) {
+          const uint64_t nmox2 = ptx::f2_pack(-mo, -mo);
+          acc2[0] = acc2[1] = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (D == 128 && c == 2) ptx::tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pall[0]));
-          uint32_t(&pk)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pall[16 * c]);
+          for (int c = 0; c < 4; ++c) {
+            if (D == 128 && allow_early && c == 2) {
+              ptx::tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pall[0]));
+              early = true;
+            }
+            uint32_t(&pk)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pall[16 * c]);
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            const uint64_t x2 = ptx::fma2(
-                ptx::f2_pack(__uint_as_float(s[c][2 * v]), __uint_as_float(s[c][2 * v + 1])),
-                sl2x2, nmox2);
-            float x0, x1;
-            ptx::f2_unpack(x2, x0, x1);
-            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-            acc2[v & 1] = ptx::add2(acc2[v & 1], ptx::f2_pack(p0, p1));
-            pk[v] = ptx::pack_x2<F16>(p0, p1);
+            for (int v = 0; v < 16; ++v) {
+              const uint64_t x2 = ptx::fma2(
+                  ptx::f2_pack(__uint_as_float(s[c][2 * v]), __uint_as_float(s[c][2 * v + 1])),
+                  sl2x2, nmox2);
+              float x0, x1;
+              ptx::f2_unpack(x2, x0, x1);
+              const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+              acc2[v & 1] = ptx::add2(acc2[v & 1], ptx::f2_pack(p0, p1));
+              pk[v] = ptx::pack_x2<F16>(p0, p1);
+            }
+          }
+        };
+        bool resc = false;
+        float alpha = 1.f;
+        bool slow = true;
+        if constexpr (C::SPEC_EXP) {
+          // After a row's first tile the exponentials run against the current
+          // reference without the tile's row maximum: P may exceed the lazy
+          // rescale's 2^8, which bf16/fp16 P and the fp32 sums absorb.  A
+          // tile sum at or above 2^15 (or not finite) sends the warp through
+          // the maximum, the rescale and the exponentials again, on S read
+          // once more from tensor memory.
+          slow = __any_sync(0xffffffffu, m_ref == -INFINITY);
+          if (!slow) {
+            exps(m_ref, false);
+            const uint64_t t2 = ptx::add2(acc2[0], acc2[1]);
+            float h0, h1;
+            ptx::f2_unpack(t2, h0, h1);
+            slow = __any_sync(0xffffffffu, !(h0 + h1 < 32768.f));
+            if (slow) load_s();
           }
         }
+        if (slow) {
+          // row maximum (minimum when scale < 0) with four independent chains
+          float a[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            a[c] = __uint_as_float(s[c][0]);
+#pragma unroll
+            for (int v = 1; v < 31; v += 2) {
+              const float x = __uint_as_float(s[c][v]), y = __uint_as_float(s[c][v + 1]);
+              a[c] = neg ? ptx::min3(a[c], x, y) : ptx::max3(a[c], x, y);
+            }
+          }
+          float mx;
+          if (!neg)
+            mx = ptx::max3(ptx::max3(a[0], a[1], __uint_as_float(s[0][31])),
+                           ptx::max3(a[2], a[3], __uint_as_float(s[1][31])),
+                           fmaxf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31])));
+          else
+            mx = ptx::min3(ptx::min3(a[0], a[1], __uint_as_float(s[0][31])),
+                           ptx::min3(a[2], a[3], __uint_as_float(s[1][31])),
+                           fminf(__uint_as_float(s[2][31]), __uint_as_float(s[3][31])));
+          const float m_cand = mx * scale_log2;
+          resc = m_cand > m_ref + FA_RESCALE_THRESHOLD;
+          if (resc) {
+            alpha = ptx::ex2(m_ref - m_cand);  // 0 on the first tile (m_ref = -inf)
+            m_ref = m_cand;
+          }
+          exps((m_ref == -INFINITY) ? 0.f : m_ref, true);
+        }
+        if constexpr (C::SPEC_EXP) signal_s_read();
         if constexpr (C::SEP_P) {
           // P_t and O_t are free once P.V_t(j-1) is done (the unit's first
           // tile: the epilogue of the previous unit waited for its last)
@@ -897,7 +946,8 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
           }
           ptx::tmem_st64(tP, pall);
         } else if constexpr (D == 128) {
-          ptx::tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pall[32]));
+          if (early) ptx::tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pall[32]));
+          else ptx::tmem_st64(tS, pall);
         } else {
           ptx::tmem_st64(tS, pall);
         }
