@@ -74,6 +74,21 @@ def test_full_parity_scale_edge_cases(cuda_lib, scale, dtype):
         check_full(o, lse, q, k, v, scale, causal, what=f"scale={scale} {dtype}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", DS)
+@pytest.mark.parametrize("ramp", [40.0, 200.0])
+def test_full_parity_row_max_jumps(cuda_lib, ramp, d, dtype):
+    """Row maxima that jump from one 128-key tile to the next by ~30 (ramp 40)
+    or ~150 (ramp 200) in log2 units: a tile exponentiated against the
+    previous reference gives P sums far above 2^15, finite or infinite, and
+    the kernel has to take the maximum, rescale and exponentiate again."""
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_structured_qkv(1, 2, 1024, d, dtype=dtype, seed=17, ramp=ramp, device="cuda")
+    for causal in (False, True):
+        o, lse = run(cuda_lib, q, k, v, causal, scale)
+        check_full(o, lse, q, k, v, scale, causal, what=f"jumps ramp={ramp} d={d} {dtype}")
+
+
 def fp32_lse_bound(q, k, scale):
     """Per-row bound on the LSE error of any fp32 evaluation (a stress-input
     tolerance, not a target one): each score is an fp32 dot product of d
