@@ -1118,18 +1118,59 @@ __global__ void __launch_bounds__(256)
   // splits [ulo + sp * chunk, ...) that hold part of [rlo, rhi)
   const int sp_first = (rlo - ulo) / chunk;
   const int ns = min(S, (rhi - ulo + chunk - 1) / chunk);
+  // four consecutive columns per lane (lanes past d re-read column 0 and
+  // store nothing)
+  const int c4 = lane * 4;
+  const bool col_ok = c4 < D;
+  const int c4c = col_ok ? c4 : 0;
+  if (ns - sp_first <= 8) {
+    // up to eight splits (the split heuristic's count): the partial-O loads
+    // go out before the L_s loads and the weights, in the same memory round
+    // trip, since they depend on neither
+    const int cnt = ns - sp_first;
+    float4 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sp = sp_first + min(u, cnt - 1);
+      x[u] = __ldg(reinterpret_cast<const float4*>(part_o + (sp * rows + row) * D + c4c));
+    }
+    const float l_mine = lane < cnt ? part_lse[(sp_first + lane) * rows + row] : -INFINITY;
+    float m8 = l_mine;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, o));
+    m8 = __shfl_sync(0xffffffffu, m8, 0);  // lanes 0-7 hold the splits
+    const float w_mine = lane < cnt ? expf(l_mine - m8) : 0.f;
+    float ws = w_mine;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    ws = __shfl_sync(0xffffffffu, ws, 0);
+    float4 a8 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = __shfl_sync(0xffffffffu, w_mine, u);  // 0 past the last split
+      a8.x = fmaf(w, x[u].x, a8.x);
+      a8.y = fmaf(w, x[u].y, a8.y);
+      a8.z = fmaf(w, x[u].z, a8.z);
+      a8.w = fmaf(w, x[u].w, a8.w);
+    }
+    const float inv8 = 1.f / ws;
+    if (col_ok) {
+      uint2 packed;
+      packed.x = ptx::pack_x2<F16>(a8.x * inv8, a8.y * inv8);
+      packed.y = ptx::pack_x2<F16>(a8.z * inv8, a8.w * inv8);
+      *reinterpret_cast<uint2*>(O + row * D + c4) = packed;
+    }
+    if (lane == 0) LSE[row] = m8 + logf(ws);
+    return;
+  }
   // m = max_s L_s over the lanes' splits sp_first + lane + 32 i
   float m = -INFINITY;
   for (int sp = sp_first + lane; sp < ns; sp += 32) m = fmaxf(m, part_lse[sp * rows + row]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  // four consecutive columns per lane (lanes past d re-read column 0 and
-  // store nothing); the weights of 32 splits at a time come from the lanes
-  // that read their L_s.  Eight splits' loads are issued together, so that
-  // each batch costs one memory round trip.
-  const int c4 = lane * 4;
-  const bool col_ok = c4 < D;
-  const int c4c = col_ok ? c4 : 0;
+  // the weights of 32 splits at a time come from the lanes that read their
+  // L_s.  Eight splits' loads are issued together, so that each batch costs
+  // one memory round trip.
   float wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int base = sp_first; base < ns; base += 32) {

@@ -176,8 +176,7 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
  * fa_fwd_split_workspace_size(B, Hq, T, d, num_splits) exceeds 64 MiB (use a
  * smaller num_splits, or 1, which needs no scratch).
  * Set-up: the first call on each device looks up the scratch array's device
- * address (cudaGetSymbolAddress, no allocation); make that first call before
- * any stream capture.  The address is cached per device together with the id
+ * address (cudaGetSymbolAddress, no allocation).  The address is cached per device together with the id
  * of the CUDA context it belongs to; after cudaDeviceReset the next call
  * finds a new context and looks the address up again.  Every call on a device shares the one array and leaves
  * its partial results there; no call relies on earlier contents, but calls

@@ -1,7 +1,7 @@
-"""The forward and backward entry points under CUDA-graph capture.
+"""fa_fwd, fa_bwd, fa_fwd_split and fa_fwd_local_global under CUDA-graph capture.
 
-No entry point allocates, frees or synchronises, so a sequence of calls can
-be captured once and replayed: the replay must give the same bits as direct
+These calls allocate, free and synchronise nothing, so a sequence of them is
+captured once and replayed: the replay must give the same bits as direct
 calls, and the same results as the fp64 oracle.
 """
 
