@@ -479,6 +479,8 @@ def run_ours(args, w):
     # forward: the C ABI's host-buffer entry point, which pipelines batch
     # chunks so that copies overlap the kernels (about 256 work units per chunk)
     chunks = max(1, min(w.B, w.B * w.Hq * ((w.T + 255) // 256) // 256))
+    if args.e2e_chunks > 0:
+        chunks = min(w.B, args.e2e_chunks)
     size_fn = fa.fa_bwd_host_workspace_size if bwd else fa.fa_fwd_host_workspace_size
     hws_bytes = size_fn(w.B, w.Hq, w.Hkv, w.T, w.d, code, chunks)
     hws = torch.empty(hws_bytes, dtype=torch.uint8, device=dev)
@@ -649,6 +651,8 @@ def main(argv=None):
     ap.add_argument("--profile", action="store_true",
                     help="device steps only (no e2e, oracle or clock sampling): for ncu")
     ap.add_argument("--B", type=int, default=0, help="override the workload's batch size")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="batch chunks of the host-buffer (e2e) leg; 0: the default rule")
     ap.add_argument("--measure-pipe-rates", action="store_true",
                     help="measure the ex2 and FMA instruction rates per clock per SM (the "
                          "denominators of the exp and fp32 rooflines) and exit")
