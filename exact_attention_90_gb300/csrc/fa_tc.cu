@@ -531,8 +531,9 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
       // One issuer per Q tile (warp 9: Q0, warp 10: Q1).  The MMA groups keep
       // the order PV0_j S0_{j+1} | PV1_j S1_{j+1} | PV0_{j+1} ... through a
       // turn word: a thread waits for its P tile and its loads first, takes
-      // its turn, issues its group, passes the turn, and only then commits,
-      // so its commits and waits overlap the other thread's MMAs.  (Two
+      // its turn, issues its group, passes the turn, and only then commits
+      // the S and K releases, so its commits and waits overlap the other
+      // thread's MMAs (the V release goes between the group's P.V and S).  (Two
       // independent issuers let the tiles fall into step and their softmax
       // warpgroups contend; the alternation keeps them half a step apart.)
       // The whole warp runs the issue loop (every branch below is warp-
@@ -705,6 +706,11 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
                                vlo + Tile::mnmajor_step(kk), Tile::DESC_HI, IDESC_PV,
                                (j > js || kk > 0) ? 1u : 0u);
             }
+            // V_j (and, after the tile's last P.V, O_t) are free once this
+            // thread's P.V is done: committed before its next S, so that the
+            // two-stage V ring reloads without waiting for that S as well
+            if (pv && j == je - 1) ptx::mma_commit_e(&bar_odone[t]);
+            if (j >= 0) ptx::mma_commit_e(&bar_vempty[cv % NSV]);
             if (sn) {
               const uint32_t klo = Tile::kmajor_lo(aK + (ck % NSK) * TILE);
 #pragma unroll
@@ -715,8 +721,6 @@ __global__ void __launch_bounds__(FA_TC_REG_SPLIT ? 384 : 352, 1)
             }
             pass_turn();
             if (sn) ptx::mma_commit_e(&bar_sfull[t]);
-            if (pv && j == je - 1) ptx::mma_commit_e(&bar_odone[t]);
-            if (j >= 0) ptx::mma_commit_e(&bar_vempty[cv % NSV]);
             if (j + 1 < u.cnt) ptx::mma_commit_e(&bar_kempty[ck % NSK]);
             // Q is free once this thread's last S of the unit is issued
             if (j + 1 == (je > js ? je - 1 : 0)) ptx::mma_commit_e(&bar_qempty[sq]);
